@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA forward prefill on GB300: one JSON line on rank 0.
+
+A step is one pass of the whole hot path (one ``kda_prefill`` call: K1 + K2 over
+every chunk of every (sequence, head), output and final state) over the
+workload's synthetic inputs, which are resident in HBM before timing starts.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--mode serial|segment] [--impl ours|reference]
+
+Multi-GPU (launched by torchrun, one rank per GPU): every rank runs its own
+independent copy of the workload (independent problems, no data-path
+collective, weak scaling); the timed region is bracketed by a barrier and a
+device synchronize, the time is the max over ranks, and ``value`` counts the
+head-tokens of all ranks.  ``--impl reference`` times the fp64 CPU oracle (the
+only reference there is) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill head-tokens/s (T·H/s) and % of roofline on 1 GB300"
+UNIT = "head-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+BYTES_PER_HEAD_TOKEN = 3 * 256 + 512 + 2 + 256   # q, k, v bf16 + g fp32 + beta + out
+STATE_BYTES = 128 * 128 * 4
+COMPUTE_DTYPE = "f32"      # arithmetic of the current serial kernel
+KERNEL_SOURCES = {"serial": ["chunked_kda_delta_gb300/csrc/kda_fwd_serial.cu"]}
+KERNEL_NAMES = {"serial": "kda_fwd_simple_kernel"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="single_t8192_h64")
+    ap.add_argument("--mode", choices=["serial", "segment"], default="serial")
+    ap.add_argument("--segment-len", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def algorithmic_bytes(w) -> int:
+    states = (1 if w.has_initial_state else 0) + 1   # read S0 (if given) + write final
+    return BYTES_PER_HEAD_TOKEN * w.head_tokens + STATE_BYTES * w.num_seqs * w.num_heads * states
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if key in d and d[key]:
+                    return float(d[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(mode: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES.get(mode, []):
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, mode: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current source."""
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(path).read()
+        m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
+        m_k = re.search(r"^source_sha256:\s*(\S+)", text, re.M)
+        m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        m_m = re.search(r"^mode:\s*(\S+)", text, re.M)
+        if m_w and m_k and m_t and m_w.group(1) == workload and \
+                (m_m is None or m_m.group(1) == mode) and m_k.group(1) == source_hash(mode):
+            return float(m_t.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.t0 = self.t1 = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        deadline = time.time() + 5
+        while not self.samples and time.time() < deadline and self.proc.poll() is None:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        time.sleep(0.12)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return None
+        inside = [s for t, s in self.samples if self.t0 and self.t0 - 0.06 <= t <= self.t1 + 0.06]
+        rows = inside or [s for _, s in self.samples][-3:]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if len(r) > 1 and num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if len(r) > 2 and num(r[2]) is not None]
+        reasons = set()
+        for r in rows:
+            for i, name in enumerate(self.NAMES):
+                if len(r) > 5 + i and r[5 + i].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples_in_timed_region": len(inside)}
+
+
+def gpu_identifier(torch, dev) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev.index or 0] if vis else str(dev.index or 0)
+
+
+def device_inputs(K, w, dev):
+    from chunked_kda_delta_gb300.inputs import make_inputs
+    inp = make_inputs(w, dev)
+    args = dict(q=inp["q"], k=inp["k"], v=inp["v"], g=inp["g"], beta=inp["beta"])
+    if w.dense:
+        B, T = w.num_seqs, w.seq_lens[0]
+        for key in ("q", "k", "v", "g"):
+            args[key] = args[key].view(B, T, w.num_heads, 128)
+        args["beta"] = args["beta"].view(B, T, w.num_heads)
+        cu = None
+    else:
+        cu = inp["cu_seqlens"]
+    return inp, args, cu
+
+
+def cpu_baseline(w, inp, seconds: float):
+    """The fp64 oracle on the host cores, over a bounded sample of the workload's heads."""
+    import oracle
+    from chunked_kda_delta_gb300.inputs import to_f64_numpy
+    lib = oracle.default()
+    cores = lib.max_threads()
+    cu = inp["cu_seqlens"].cpu().numpy().astype("int64")
+    done_heads, head_tokens, elapsed = 0, 0, 0.0
+    while done_heads < w.num_heads and elapsed < seconds:
+        hs = list(range(done_heads, min(w.num_heads, done_heads + cores)))
+        sel = {k: to_f64_numpy(inp[k][:, hs]) for k in ("q", "k", "v", "g", "beta")}
+        s0 = None if inp["initial_state"] is None else to_f64_numpy(inp["initial_state"][:, hs])
+        t = time.perf_counter()
+        lib.recurrent(sel["q"], sel["k"], sel["v"], sel["g"], sel["beta"], inp["scale"], s0=s0,
+                      cu_seqlens=cu)
+        elapsed += time.perf_counter() - t
+        done_heads += len(hs)
+        head_tokens += w.total_tokens * len(hs)
+    return {"value": head_tokens / elapsed, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done_heads} of {w.num_heads} heads x all {w.total_tokens} tokens "
+                      f"(fp64 token-by-token recurrence, {elapsed:.1f} s)"}
+
+
+def run_reference(args, w):
+    """Reference arm: the fp64 CPU oracle as it stands, on bounded samples of the workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from chunked_kda_delta_gb300.inputs import make_inputs, to_f64_numpy
+    lib = oracle.default()
+    cores = lib.max_threads()
+    # Inputs for a prefix of every head (the recurrence cost is the same for every token).
+    budget = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    probe_tokens = min(w.seq_lens[0] if w.seq_lens[0] > 0 else 1, 256)
+    inp = make_inputs(w, "cpu")
+    hs = list(range(min(w.num_heads, cores)))
+    def sample(tokens):
+        lens = []
+        left = tokens
+        for L in w.seq_lens:
+            take = min(L, left)
+            lens.append(take)
+            left -= take
+        idx = np.concatenate([np.arange(c, c + t) for c, t in
+                              zip(np.cumsum([0] + list(w.seq_lens[:-1])), lens)])
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        d = {k: to_f64_numpy(inp[k][idx][:, hs]) for k in ("q", "k", "v", "g", "beta")}
+        s0 = None if inp["initial_state"] is None else to_f64_numpy(inp["initial_state"][:, hs])
+        return d, s0, cu, sum(lens)
+    d, s0, cu, nt = sample(probe_tokens)
+    t = time.perf_counter()
+    lib.recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], s0=s0, cu_seqlens=cu)
+    per_token = (time.perf_counter() - t) / max(1, nt)
+    tokens = int(max(1, min(w.total_tokens, budget / max(per_token, 1e-9))))
+    d, s0, cu, nt = sample(tokens)
+    def step():
+        lib.recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], s0=s0,
+                      cu_seqlens=cu)
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    total = time.perf_counter() - t
+    ht = nt * len(hs)
+    value = ht * args.steps / total
+    desc = (f"{len(hs)} of {w.num_heads} heads x first {nt} of {w.total_tokens} tokens per step "
+            f"(fp64 token-by-token recurrence)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, args, note="CPU oracle on a bounded sample per step"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def workload_config(w, args, note=None):
+    cfg = {"workload": w.name, "seq_lens": (list(w.seq_lens) if len(w.seq_lens) <= 4 else
+                                            f"{w.num_seqs} sequences, {w.total_tokens} tokens"),
+           "num_heads": w.num_heads, "head_dim": 128, "chunk": 16,
+           "initial_state": w.has_initial_state, "final_state": True, "mode": args.mode,
+           "head_tokens_per_gpu": w.head_tokens, "parallelism": f"replicas x{args.gpus}",
+           "l2": "no flush; inputs larger than L2 "
+                 f"({algorithmic_bytes(w) / 1e6:.0f} MB per step vs 129 MB)"}
+    if note:
+        cfg["note"] = note
+    return cfg
+
+
+def main():
+    args = parse_args()
+    from chunked_kda_delta_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+    import torch
+    import chunked_kda_delta_gb300 as K
+    from chunked_kda_delta_gb300 import build as kbuild
+
+    rank, world, local = dist_env()
+    kbuild.build()
+    K.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    mode = K.MODE_SEGMENT if args.mode == "segment" else K.MODE_SERIAL
+    inp, a, cu = device_inputs(K, w, dev)
+    N = w.num_seqs
+    out = torch.empty_like(a["q"])
+    fin = torch.empty((N, w.num_heads, 128, 128), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        K.kda_prefill(**a, scale=inp["scale"], initial_state=inp["initial_state"], cu_seqlens=cu,
+                      out=out, final_state=fin, stream=stream, mode=mode,
+                      segment_len=args.segment_len)
+
+    clocks = ClockSampler(gpu_identifier(torch, dev))
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if K.kda_get_device_status() != 0:
+        raise RuntimeError("device status error after warm-up")
+    launches_per_step = 1
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    if pg:
+        pg.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kernel_ms = statistics.mean(s.elapsed_time(e) for s, e in evs)
+    if K.kda_get_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    if pg:
+        t = torch.tensor([elapsed_ms, kernel_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms, kernel_ms = float(t[0]), float(t[1])
+    value = world * w.head_tokens * args.steps / (elapsed_ms / 1e3)
+
+    e2e = None
+    if not args.no_e2e:
+        host = {k: inp[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
+        s0h = None if inp["initial_state"] is None else inp["initial_state"].cpu().pin_memory()
+        cuh = None if cu is None else cu.cpu()
+        if w.dense:
+            B, T = w.num_seqs, w.seq_lens[0]
+            for key in ("q", "k", "v", "g"):
+                host[key] = host[key].view(B, T, w.num_heads, 128)
+            host["beta"] = host["beta"].view(B, T, w.num_heads)
+        oh = torch.empty(host["q"].shape, dtype=torch.bfloat16).pin_memory()
+        fh = torch.empty((N, w.num_heads, 128, 128), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            K.kda_prefill_host(**host, scale=inp["scale"], initial_state=s0h, cu_seqlens=cuh,
+                               out=oh, final_state=fh, mode=mode, segment_len=args.segment_len)
+        e2e_step()
+        if pg:
+            pg.barrier()
+        t = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t) / args.e2e_steps
+        if pg:
+            tt = torch.tensor([e2e_s], device=dev)
+            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+            e2e_s = float(tt[0])
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
+        h2d += 0 if s0h is None else s0h.numel() * 4
+        h2d += 0 if cuh is None else cuh.numel() * 4
+        d2h = oh.numel() * 2 + fh.numel() * 4
+        e2e = {"value": world * w.head_tokens / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp, args.cpu_seconds)
+
+    if rank == 0:
+        peak, peak_kind = measured_peaks()
+        algo = algorithmic_bytes(w)
+        achieved = algo / (kernel_ms / 1e3) / 1e9
+        traffic = recorded_traffic(w.name, args.mode)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": COMPUTE_DTYPE, "data": "synthetic",
+            "config": workload_config(w, args),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} HBM copy bandwidth",
+                         "kernel": KERNEL_NAMES.get(args.mode, args.mode),
+                         "kernel_ms": kernel_ms, "algorithmic_bytes_per_launch": algo},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line))
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

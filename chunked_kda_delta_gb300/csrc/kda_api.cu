@@ -1,0 +1,473 @@
+// kda_api.cu -- the C ABI (include/kda.h): validation, device cache, workspaces,
+// launch and status reporting.  Host code only; the kernels live in their own
+// translation units and are reached through kda_internal.cuh.
+//
+// Conventions follow the pages' reviews of the reference bindings: per-device
+// queries are cached instead of repeated on every launch (flashinfer PR #4313,
+// review of the FlashKDA binding's per-launch capability checks); scratch is
+// keyed by (device, stream) so concurrent streams never share it and is
+// bounded (cuLA PR #103, review of the "_get_scratch" cache); an exact alias of
+// the initial and final state is allowed for in-place updates, any partial
+// overlap is rejected (flashinfer PR #4351, review of the overlap checks).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+kda_status fail(kda_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kda_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(KDA_ERR_CUDA, "%s failed: %s", what, cudaGetErrorString(e));
+}
+
+__device__ int32_t g_status_word = 0;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kDefaultWaitLimit = 1ll << 26;
+constexpr size_t kMaxWorkspaces = 8;
+
+struct DeviceInfo {
+    bool ready = false;
+    int cc_major = 0, cc_minor = 0, sm_count = 0;
+    int32_t* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+
+kda_status device_info(int dev, DeviceInfo** out) {
+    if (dev < 0 || dev >= kMaxDevices) return fail(KDA_ERR_UNSUPPORTED_DEVICE, "device %d", dev);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready) {
+        cudaError_t e;
+        if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+            (e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)))
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (d.cc_major != 10 || d.cc_minor != 3)
+            return fail(KDA_ERR_UNSUPPORTED_DEVICE,
+                        "device %d has compute capability %d.%d; this library is built for "
+                        "sm_103a (10.3) only", dev, d.cc_major, d.cc_minor);
+        if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word)))
+            return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+        if ((e = cudaFuncSetAttribute(kda::serial_kernel_symbol(),
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kda::serial_smem_bytes())))
+            return cuda_fail(e, "cudaFuncSetAttribute(serial kernel)");
+        d.ready = true;
+    }
+    *out = &d;
+    return KDA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Workspaces: one device buffer per (device, stream), grown on demand, at most
+// kMaxWorkspaces alive (least recently used evicted).
+enum WorkspaceKind { kWsSegment = 0, kWsHostArena = 1 };
+
+struct Workspace {
+    int device;
+    void* stream;
+    int kind;
+    void* ptr;
+    size_t bytes;
+    unsigned long long last_use;
+};
+std::vector<Workspace> g_workspaces;
+unsigned long long g_use_clock = 0;
+
+kda_status get_workspace(int dev, cudaStream_t stream, int kind, size_t bytes, void** out) {
+    *out = nullptr;
+    if (bytes == 0) return KDA_OK;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (auto& w : g_workspaces)
+        if (w.device == dev && w.stream == (void*)stream && w.kind == kind && w.bytes >= bytes) {
+            w.last_use = ++g_use_clock;
+            *out = w.ptr;
+            return KDA_OK;
+        }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone)
+        return fail(KDA_ERR_CAPTURE_NEEDS_WARMUP,
+                    "a %zu-byte workspace is needed while the stream is being captured; run "
+                    "the same call once before capture", bytes);
+    // Replace a smaller buffer of the same key, else evict the LRU entry when full.
+    for (size_t i = 0; i < g_workspaces.size(); ++i)
+        if (g_workspaces[i].device == dev && g_workspaces[i].stream == (void*)stream &&
+            g_workspaces[i].kind == kind) {
+            cudaStreamSynchronize(stream);
+            cudaFree(g_workspaces[i].ptr);
+            g_workspaces.erase(g_workspaces.begin() + i);
+            break;
+        }
+    if (g_workspaces.size() >= kMaxWorkspaces) {
+        size_t lru = 0;
+        for (size_t i = 1; i < g_workspaces.size(); ++i)
+            if (g_workspaces[i].last_use < g_workspaces[lru].last_use) lru = i;
+        int cur;
+        cudaGetDevice(&cur);
+        cudaSetDevice(g_workspaces[lru].device);
+        cudaDeviceSynchronize();
+        cudaFree(g_workspaces[lru].ptr);
+        cudaSetDevice(cur);
+        g_workspaces.erase(g_workspaces.begin() + lru);
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(KDA_ERR_OUT_OF_MEMORY, "cudaMalloc(%zu) for a workspace failed: %s", bytes,
+                    cudaGetErrorString(e));
+    }
+    g_workspaces.push_back({dev, (void*)stream, kind, p, bytes, ++g_use_clock});
+    *out = p;
+    return KDA_OK;
+}
+
+// ---------------------------------------------------------------------------
+struct Range {
+    const void* p;
+    size_t bytes;
+};
+
+bool overlaps(Range a, Range b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+struct Problem {
+    int64_t T_total, dense_len;
+    int32_t N, H;
+    bool varlen;
+};
+
+kda_status validate_shape(const kda_shape* s, bool varlen, Problem* pr) {
+    if (!s) return fail(KDA_ERR_INVALID_ARGUMENT, "shape is NULL");
+    if (s->head_dim != kda::kD)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "head_dim must be 128 (got %d)", s->head_dim);
+    if (s->num_heads <= 0)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "num_heads must be >= 1 (got %d)", s->num_heads);
+    if (s->seq_len < 0)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "seq_len must be >= 0 (got %lld)",
+                    (long long)s->seq_len);
+    pr->H = s->num_heads;
+    pr->varlen = varlen;
+    if (varlen) {
+        if (s->batch != 1)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "packed varlen input needs batch == 1 (got %d)",
+                        s->batch);
+        if (s->num_seqs <= 0)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "num_seqs must be >= 1 with cu_seqlens (got %d)",
+                        s->num_seqs);
+        pr->N = s->num_seqs;
+        pr->T_total = s->seq_len;
+        pr->dense_len = 0;
+    } else {
+        if (s->batch <= 0)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "batch must be >= 1 (got %d)", s->batch);
+        pr->N = s->batch;
+        pr->dense_len = s->seq_len;
+        if (s->seq_len > (int64_t)1 << 40)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "seq_len too large");
+        pr->T_total = (int64_t)s->batch * s->seq_len;
+    }
+    if ((int64_t)pr->N * pr->H > 0x7fffffffll)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "num_seqs * num_heads exceeds 2^31 - 1");
+    if (pr->T_total > ((int64_t)1 << 46) / ((int64_t)pr->H * kda::kD))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "T_total * H * 128 is too large");
+    return KDA_OK;
+}
+
+kda_status validate_options(const kda_options* o, const Problem& pr, int32_t* mode,
+                            int32_t* seg_len, int64_t* wait_limit) {
+    *mode = KDA_MODE_SERIAL;
+    *seg_len = 8192;
+    *wait_limit = kDefaultWaitLimit;
+    if (!o) return KDA_OK;
+    if (o->mode != KDA_MODE_SERIAL && o->mode != KDA_MODE_SEGMENT && o->mode != KDA_MODE_AUTO)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "unknown mode %d", o->mode);
+    if (o->segment_len < 0 || (o->segment_len % kda::kChunk) != 0)
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "segment_len must be a non-negative multiple of 16 (got %d)", o->segment_len);
+    if (o->wait_limit < 0)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "wait_limit must be >= 0");
+    if (o->mode == KDA_MODE_SEGMENT && pr.varlen)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "segment mode needs dense input (no cu_seqlens)");
+    *mode = o->mode;
+    if (o->segment_len) *seg_len = o->segment_len;
+    if (o->wait_limit) *wait_limit = o->wait_limit;
+    return KDA_OK;
+}
+
+kda_status validate_pointers(const Problem& pr, const uint16_t* q, const uint16_t* k,
+                             const uint16_t* v, const float* g, const uint16_t* beta, float scale,
+                             const float* s0, const int32_t* cu, const uint16_t* out,
+                             const float* sfin) {
+    if (!(scale == scale) || scale > 3.4e38f || scale < -3.4e38f)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "scale must be finite");
+    const size_t x2 = (size_t)pr.T_total * pr.H * kda::kD * 2;
+    const size_t x4 = x2 * 2;
+    const size_t b2 = (size_t)pr.T_total * pr.H * 2;
+    const size_t st = (size_t)pr.N * pr.H * kda::kD * kda::kD * 4;
+    const size_t cub = pr.varlen ? (size_t)(pr.N + 1) * 4 : 0;
+    if (pr.T_total > 0) {
+        const void* req[] = {q, k, v, g, beta, out};
+        const char* names[] = {"q", "k", "v", "g", "beta", "out"};
+        for (int i = 0; i < 6; ++i)
+            if (!req[i]) return fail(KDA_ERR_INVALID_ARGUMENT, "%s is NULL", names[i]);
+        const void* al16[] = {q, k, v, g, out};
+        const char* n16[] = {"q", "k", "v", "g", "out"};
+        for (int i = 0; i < 5; ++i)
+            if (!aligned(al16[i], 16))
+                return fail(KDA_ERR_INVALID_ARGUMENT, "%s must be 16-byte aligned", n16[i]);
+        if (!aligned(beta, 2)) return fail(KDA_ERR_INVALID_ARGUMENT, "beta must be 2-byte aligned");
+    }
+    if (pr.varlen && !cu) return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens is NULL");
+    if (cu && !aligned(cu, 4)) return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must be 4-byte aligned");
+    if (s0 && !aligned(s0, 16))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "initial_state must be 16-byte aligned");
+    if (sfin && !aligned(sfin, 16))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "final_state must be 16-byte aligned");
+
+    const Range rq{q, x2}, rk{k, x2}, rv{v, x2}, rg{g, x4}, rb{beta, b2}, rs0{s0, st},
+        rcu{cu, cub}, rout{out, x2}, rfin{sfin, st};
+    const Range ins[] = {rq, rk, rv, rg, rb, rs0, rcu, rfin};
+    const char* in_names[] = {"q", "k", "v", "g", "beta", "initial_state", "cu_seqlens",
+                              "final_state"};
+    for (int i = 0; i < 8; ++i)
+        if (overlaps(rout, ins[i]))
+            return fail(KDA_ERR_ALIASING, "out overlaps %s", in_names[i]);
+    const Range fin_ins[] = {rq, rk, rv, rg, rb, rcu};
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(rfin, fin_ins[i]))
+            return fail(KDA_ERR_ALIASING, "final_state overlaps %s", in_names[i]);
+    if (s0 && sfin && s0 != sfin && overlaps(rs0, rfin))
+        return fail(KDA_ERR_ALIASING,
+                    "initial_state and final_state overlap without being the same buffer");
+    return KDA_OK;
+}
+
+kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+               const float* g, const uint16_t* beta, float scale, const float* s0,
+               const int32_t* cu, uint16_t* out, float* sfin, cudaStream_t stream,
+               int32_t mode, int32_t seg_len, int64_t wait_limit) {
+    (void)seg_len;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo* di = nullptr;
+    kda_status st = device_info(dev, &di);
+    if (st != KDA_OK) return st;
+    if (pr.T_total == 0 && !sfin) return KDA_OK;
+
+    kda::FwdParams p{};
+    p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16*>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16*>(v);
+    p.g = g;
+    p.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
+    p.s0 = s0;
+    p.sfin = sfin;
+    p.out = reinterpret_cast<__nv_bfloat16*>(out);
+    p.cu = cu;
+    p.T_total = pr.T_total;
+    p.dense_len = pr.dense_len;
+    p.N = pr.N;
+    p.H = pr.H;
+    p.scale = scale;
+    p.wait_limit = wait_limit;
+    p.status = di->status;
+    (void)mode;
+    e = kda::launch_serial(p, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "serial prefill launch");
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill_ex(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
+                          const uint16_t* v, const float* g, const uint16_t* beta, float scale,
+                          const float* initial_state, const int32_t* cu_seqlens, uint16_t* out,
+                          float* final_state, void* stream, const kda_options* opts) {
+    t_last_error[0] = '\0';
+    Problem pr{};
+    kda_status st = validate_shape(shape, cu_seqlens != nullptr, &pr);
+    if (st != KDA_OK) return st;
+    int32_t mode, seg_len;
+    int64_t wait_limit;
+    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit)) != KDA_OK) return st;
+    if ((st = validate_pointers(pr, q, k, v, g, beta, scale, initial_state, cu_seqlens, out,
+                                final_state)) != KDA_OK)
+        return st;
+    return run(pr, q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
+               (cudaStream_t)stream, mode, seg_len, wait_limit);
+}
+
+kda_status kda_prefill(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
+                       const uint16_t* v, const float* g, const uint16_t* beta, float scale,
+                       const float* initial_state, const int32_t* cu_seqlens, uint16_t* out,
+                       float* final_state, void* stream) {
+    return kda_prefill_ex(shape, q, k, v, g, beta, scale, initial_state, cu_seqlens, out,
+                          final_state, stream, nullptr);
+}
+
+kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
+                            const uint16_t* v, const float* g, const uint16_t* beta,
+                            float scale, const float* initial_state,
+                            const int32_t* cu_seqlens, uint16_t* out, float* final_state,
+                            void* stream_, const kda_options* opts) {
+    t_last_error[0] = '\0';
+    cudaStream_t stream = (cudaStream_t)stream_;
+    Problem pr{};
+    kda_status st = validate_shape(shape, cu_seqlens != nullptr, &pr);
+    if (st != KDA_OK) return st;
+    int32_t mode, seg_len;
+    int64_t wait_limit;
+    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit)) != KDA_OK) return st;
+    if (pr.T_total > 0 && (!q || !k || !v || !g || !beta || !out))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "a required host pointer is NULL");
+    if (pr.varlen) {  // host copy of the offsets: check them here
+        if (cu_seqlens[0] != 0 || cu_seqlens[pr.N] != pr.T_total)
+            return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must start at 0 and end at T_total");
+        for (int n = 0; n < pr.N; ++n)
+            if (cu_seqlens[n + 1] < cu_seqlens[n])
+                return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must be non-decreasing");
+    }
+    const size_t x2 = (size_t)pr.T_total * pr.H * kda::kD * 2;
+    const size_t x4 = x2 * 2;
+    const size_t b2 = (size_t)pr.T_total * pr.H * 2;
+    const size_t sb = (size_t)pr.N * pr.H * kda::kD * kda::kD * 4;
+    const size_t cub = pr.varlen ? (size_t)(pr.N + 1) * 4 : 0;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t off_q = 0, off_k = off_q + up(x2), off_v = off_k + up(x2), off_g = off_v + up(x2),
+                 off_b = off_g + up(x4), off_s0 = off_b + up(b2),
+                 off_cu = off_s0 + (initial_state ? up(sb) : 0), off_out = off_cu + up(cub),
+                 off_fin = off_out + up(x2), total = off_fin + (final_state ? up(sb) : 0);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo* di = nullptr;
+    if ((st = device_info(dev, &di)) != KDA_OK) return st;
+    void* base = nullptr;
+    if ((st = get_workspace(dev, stream, kWsHostArena, total, &base)) != KDA_OK)
+        return st;
+    char* b = static_cast<char*>(base);
+    struct Cp {
+        void* dst;
+        const void* src;
+        size_t n;
+    } ins[] = {{b + off_q, q, x2},  {b + off_k, k, x2},  {b + off_v, v, x2},
+               {b + off_g, g, x4},  {b + off_b, beta, b2},
+               {b + off_s0, initial_state, initial_state ? sb : 0},
+               {b + off_cu, cu_seqlens, cub}};
+    for (auto& c : ins)
+        if (c.n && (e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, stream)))
+            return cuda_fail(e, "cudaMemcpyAsync host->device");
+    uint16_t* d_out = reinterpret_cast<uint16_t*>(b + off_out);
+    float* d_fin = final_state ? reinterpret_cast<float*>(b + off_fin) : nullptr;
+    st = run(pr, reinterpret_cast<uint16_t*>(b + off_q), reinterpret_cast<uint16_t*>(b + off_k),
+             reinterpret_cast<uint16_t*>(b + off_v), reinterpret_cast<float*>(b + off_g),
+             reinterpret_cast<uint16_t*>(b + off_b),
+             scale, initial_state ? reinterpret_cast<float*>(b + off_s0) : nullptr,
+             pr.varlen ? reinterpret_cast<int32_t*>(b + off_cu) : nullptr, d_out, d_fin, stream,
+             mode, seg_len, wait_limit);
+    if (st != KDA_OK) return st;
+    if (x2 && (e = cudaMemcpyAsync(out, d_out, x2, cudaMemcpyDeviceToHost, stream)))
+        return cuda_fail(e, "cudaMemcpyAsync device->host (out)");
+    if (d_fin && (e = cudaMemcpyAsync(final_state, d_fin, sb, cudaMemcpyDeviceToHost, stream)))
+        return cuda_fail(e, "cudaMemcpyAsync device->host (final_state)");
+    if ((e = cudaStreamSynchronize(stream))) return cuda_fail(e, "cudaStreamSynchronize");
+    return KDA_OK;
+}
+
+kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, size_t* bytes) {
+    t_last_error[0] = '\0';
+    if (!bytes) return fail(KDA_ERR_INVALID_ARGUMENT, "bytes is NULL");
+    Problem pr{};
+    kda_status st = validate_shape(shape, false, &pr);
+    if (st != KDA_OK) return st;
+    int32_t mode, seg_len;
+    int64_t wait_limit;
+    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit)) != KDA_OK) return st;
+    *bytes = 0;
+    return KDA_OK;
+}
+
+kda_status kda_get_device_status(void* stream, int32_t* code) {
+    t_last_error[0] = '\0';
+    if (!code) return fail(KDA_ERR_INVALID_ARGUMENT, "code is NULL");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo* di = nullptr;
+    kda_status st = device_info(dev, &di);
+    if (st != KDA_OK) return st;
+    if ((e = cudaStreamSynchronize((cudaStream_t)stream))) return cuda_fail(e, "cudaStreamSynchronize");
+    int32_t host = 0;
+    if ((e = cudaMemcpy(&host, di->status, sizeof(host), cudaMemcpyDeviceToHost)))
+        return cuda_fail(e, "cudaMemcpy(status word)");
+    const int32_t zero = 0;
+    if ((e = cudaMemcpy(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice)))
+        return cuda_fail(e, "cudaMemcpy(status word reset)");
+    *code = host;
+    return KDA_OK;
+}
+
+kda_status kda_release_workspaces(int32_t device) {
+    t_last_error[0] = '\0';
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (size_t i = 0; i < g_workspaces.size();) {
+        if (device < 0 || g_workspaces[i].device == device) {
+            cudaSetDevice(g_workspaces[i].device);
+            cudaDeviceSynchronize();
+            cudaFree(g_workspaces[i].ptr);
+            g_workspaces.erase(g_workspaces.begin() + i);
+        } else {
+            ++i;
+        }
+    }
+    cudaSetDevice(cur);
+    return KDA_OK;
+}
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+        case KDA_ERR_ALIASING: return "KDA_ERR_ALIASING";
+        case KDA_ERR_UNSUPPORTED_DEVICE: return "KDA_ERR_UNSUPPORTED_DEVICE";
+        case KDA_ERR_OUT_OF_MEMORY: return "KDA_ERR_OUT_OF_MEMORY";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_CAPTURE_NEEDS_WARMUP: return "KDA_ERR_CAPTURE_NEEDS_WARMUP";
+        case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_last_error_message(void) { return t_last_error; }
+
+const char* kda_version(void) { return "0.1.0"; }
+
+}  // extern "C"

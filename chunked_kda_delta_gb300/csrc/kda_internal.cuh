@@ -1,0 +1,62 @@
+// kda_internal.cuh -- declarations shared by the library's translation units
+// (host API and kernels).  Not part of the public ABI; see include/kda.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kD = 128;     // Dk = Dv
+constexpr int kChunk = 16;  // rows per chunk
+
+// Device status codes (same values as kda_status).
+constexpr int32_t kStatusOk = 0;
+constexpr int32_t kStatusBadSeqlens = 1;
+constexpr int32_t kStatusTimeout = 7;
+
+// Everything a forward launch needs; plain pointers and sizes.
+struct FwdParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* g;
+    const __nv_bfloat16* beta;
+    const float* s0;      // [N][H][128][128] or nullptr (zero state)
+    float* sfin;          // [N][H][128][128] or nullptr (not written)
+    __nv_bfloat16* out;   // [T_total][H][128]
+    const int32_t* cu;    // [N + 1] or nullptr (dense)
+    int64_t T_total;
+    int64_t dense_len;    // tokens per sequence when cu == nullptr
+    int32_t N;
+    int32_t H;
+    float scale;
+    int64_t wait_limit;   // iteration limit of bounded spin waits
+    int32_t* status;      // device status word of this device
+};
+
+// Token range [bos, eos) of sequence n; false (and the status word set) when
+// cu_seqlens is malformed for this sequence.
+__device__ __forceinline__ bool seq_range(const FwdParams& p, int n, int64_t& bos,
+                                          int64_t& eos) {
+    if (p.cu == nullptr) {
+        bos = (int64_t)n * p.dense_len;
+        eos = bos + p.dense_len;
+        return true;
+    }
+    bos = p.cu[n];
+    eos = p.cu[n + 1];
+    if ((n == 0 && bos != 0) || bos < 0 || eos < bos || eos > p.T_total) {
+        atomicCAS(p.status, kStatusOk, kStatusBadSeqlens);
+        return false;
+    }
+    return true;
+}
+
+// Launchers (return the launch error, cudaSuccess on success).
+cudaError_t launch_serial(const FwdParams& p, cudaStream_t stream);
+size_t serial_smem_bytes();
+const void* serial_kernel_symbol();
+
+}  // namespace kda

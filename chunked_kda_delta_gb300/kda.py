@@ -1,0 +1,267 @@
+"""Thin Python binding of the KDA C ABI (``include/kda.h``) through ctypes.
+
+Argument marshalling only: tensors are checked for dtype, layout and device,
+their pointers and sizes are passed to ``libkda.so`` and every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: if the
+compiled library is missing or the call fails, :class:`KdaError` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MODE_SERIAL = 0
+MODE_SEGMENT = 1
+MODE_AUTO = 2
+
+_STATUS = {
+    0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_ALIASING",
+    3: "KDA_ERR_UNSUPPORTED_DEVICE", 4: "KDA_ERR_OUT_OF_MEMORY", 5: "KDA_ERR_CUDA",
+    6: "KDA_ERR_CAPTURE_NEEDS_WARMUP", 7: "KDA_ERR_DEVICE_TIMEOUT",
+}
+
+EXPORTED_SYMBOLS = (
+    "kda_prefill", "kda_prefill_ex", "kda_prefill_host", "kda_workspace_bytes",
+    "kda_get_device_status", "kda_release_workspaces", "kda_status_string",
+    "kda_last_error_message", "kda_version",
+)
+
+
+class KdaError(RuntimeError):
+    """A non-OK status from the library (``status`` holds the code)."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class KdaShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("seq_len", ctypes.c_int64),
+                ("num_seqs", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32)]
+
+
+class KdaOptions(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("segment_len", ctypes.c_int32),
+                ("wait_limit", ctypes.c_int64)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: Optional[str] = None, build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load ``libkda.so`` (built by :mod:`chunked_kda_delta_gb300.build`)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            if build_if_missing:
+                p = _build.build()
+            else:
+                raise KdaError(5, f"CUDA library {p} is missing; build it with "
+                                  "`python -m chunked_kda_delta_gb300.build`")
+        lib = ctypes.CDLL(p)
+        vp, u16p, f32p, i32p = (ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_void_p)
+        args = [ctypes.POINTER(KdaShape), u16p, u16p, u16p, f32p, u16p, ctypes.c_float,
+                f32p, i32p, u16p, f32p, vp]
+        lib.kda_prefill.argtypes = args
+        lib.kda_prefill_ex.argtypes = args + [ctypes.POINTER(KdaOptions)]
+        lib.kda_prefill_host.argtypes = args + [ctypes.POINTER(KdaOptions)]
+        lib.kda_workspace_bytes.argtypes = [ctypes.POINTER(KdaShape), ctypes.POINTER(KdaOptions),
+                                            ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.kda_release_workspaces.argtypes = [ctypes.c_int32]
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_last_error_message.restype = ctypes.c_char_p
+        lib.kda_version.restype = ctypes.c_char_p
+        for f in (lib.kda_prefill, lib.kda_prefill_ex, lib.kda_prefill_host,
+                  lib.kda_workspace_bytes, lib.kda_get_device_status,
+                  lib.kda_release_workspaces):
+            f.restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(lib, status: int):
+    if status != 0:
+        raise KdaError(status, lib.kda_last_error_message().decode())
+
+
+def kda_status_string(status: int) -> str:
+    return load_library().kda_status_string(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _shape_of(q: torch.Tensor, cu_seqlens) -> KdaShape:
+    if q.dim() == 4:
+        B, T, H, D = q.shape
+    elif q.dim() == 3:
+        B, (T, H, D) = 1, q.shape
+    else:
+        raise ValueError("q must be [T, H, 128] or [B, T, H, 128]")
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("packed varlen input needs batch 1")
+        return KdaShape(1, T, cu_seqlens.numel() - 1, H, D)
+    return KdaShape(B, T, 0, H, D)
+
+
+def _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, device_type):
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("g", g, torch.float32),
+                        ("beta", beta, torch.bfloat16)):
+        if t.dtype != dt:
+            raise ValueError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device.type != device_type:
+            raise ValueError(f"{name} must be on {device_type}")
+    if q.shape != k.shape or q.shape != v.shape or q.shape != g.shape:
+        raise ValueError("q, k, v, g must share one shape")
+    if beta.shape != q.shape[:-1]:
+        raise ValueError("beta must have q's shape without the last dim")
+    if initial_state is not None:
+        if initial_state.dtype != torch.float32 or not initial_state.is_contiguous():
+            raise ValueError("initial_state must be contiguous float32")
+        if initial_state.device.type != device_type:
+            raise ValueError(f"initial_state must be on {device_type}")
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_contiguous():
+            raise ValueError("cu_seqlens must be contiguous int32")
+        if cu_seqlens.device.type != device_type:
+            raise ValueError(f"cu_seqlens must be on {device_type}")
+
+
+def _options(mode, segment_len, wait_limit):
+    return KdaOptions(int(mode), int(segment_len), int(wait_limit))
+
+
+def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                beta: torch.Tensor, scale: Optional[float] = None,
+                initial_state: Optional[torch.Tensor] = None,
+                cu_seqlens: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None,
+                final_state: Optional[torch.Tensor] = None,
+                stream=None, output_final_state: bool = False,
+                mode: int = MODE_SERIAL, segment_len: int = 0, wait_limit: int = 0):
+    """KDA forward prefill on CUDA tensors; returns ``(out, final_state)``.
+
+    q, k, v: bf16 ``[T, H, 128]`` (or ``[B, T, H, 128]`` dense); g: fp32 of the
+    same shape; beta: bf16 ``[T, H]``; initial_state / final_state: fp32
+    ``[N, H, 128, 128]``; cu_seqlens: int32 ``[N + 1]`` on the device.  ``out``
+    is allocated when not given; ``final_state`` is allocated when
+    ``output_final_state`` is set and none is given (pass ``final_state =
+    initial_state`` to update in place).  The call is asynchronous on
+    ``stream`` (a ``torch.cuda.Stream``, a raw handle, or the current stream).
+    """
+    lib = load_library()
+    _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, "cuda")
+    shape = _shape_of(q, cu_seqlens)
+    N = shape.num_seqs if cu_seqlens is not None else shape.batch
+    if scale is None:
+        scale = shape.head_dim ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, shape.num_heads, shape.head_dim, shape.head_dim),
+                                  dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    opts = _options(mode, segment_len, wait_limit)
+    with torch.cuda.device(q.device):
+        st = lib.kda_prefill_ex(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                _ptr(beta), ctypes.c_float(scale), _ptr(initial_state),
+                                _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                ctypes.c_void_p(int(stream)), ctypes.byref(opts))
+    _check(lib, st)
+    return out, final_state
+
+
+def kda_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                     beta: torch.Tensor, scale: Optional[float] = None,
+                     initial_state: Optional[torch.Tensor] = None,
+                     cu_seqlens: Optional[torch.Tensor] = None,
+                     out: Optional[torch.Tensor] = None,
+                     final_state: Optional[torch.Tensor] = None,
+                     stream=None, output_final_state: bool = False, device=None,
+                     mode: int = MODE_SERIAL, segment_len: int = 0, wait_limit: int = 0):
+    """End-to-end prefill on HOST (CPU) tensors: copy in, compute, copy out, synchronise.
+
+    Same arguments as :func:`kda_prefill` but every tensor lives in host memory
+    (pinned memory gives full copy bandwidth); ``device`` picks the GPU.
+    """
+    lib = load_library()
+    _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, "cpu")
+    shape = _shape_of(q, cu_seqlens)
+    N = shape.num_seqs if cu_seqlens is not None else shape.batch
+    if scale is None:
+        scale = shape.head_dim ** -0.5
+    if out is None:
+        out = torch.empty_like(q, pin_memory=q.is_pinned())
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, shape.num_heads, shape.head_dim, shape.head_dim),
+                                  dtype=torch.float32, pin_memory=q.is_pinned())
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    opts = _options(mode, segment_len, wait_limit)
+    with torch.cuda.device(dev):
+        st = lib.kda_prefill_host(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                  _ptr(beta), ctypes.c_float(scale), _ptr(initial_state),
+                                  _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                  ctypes.c_void_p(int(stream)), ctypes.byref(opts))
+    _check(lib, st)
+    return out, final_state
+
+
+def kda_workspace_bytes(batch: int, seq_len: int, num_heads: int, mode: int = MODE_SERIAL,
+                        segment_len: int = 0, head_dim: int = 128) -> int:
+    """Device workspace bytes for a dense problem of this shape in this mode."""
+    lib = load_library()
+    shape = KdaShape(batch, seq_len, 0, num_heads, head_dim)
+    opts = _options(mode, segment_len, 0)
+    n = ctypes.c_size_t(0)
+    _check(lib, lib.kda_workspace_bytes(ctypes.byref(shape), ctypes.byref(opts),
+                                        ctypes.byref(n)))
+    return int(n.value)
+
+
+def kda_get_device_status(stream=None, device=None) -> int:
+    """Synchronise ``stream`` and read-and-clear the device status word (0 = OK)."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    code = ctypes.c_int32(0)
+    with torch.cuda.device(dev):
+        _check(lib, lib.kda_get_device_status(ctypes.c_void_p(int(stream)), ctypes.byref(code)))
+    return int(code.value)
+
+
+def kda_release_workspaces(device: int = -1) -> None:
+    """Free the library's workspaces on ``device`` (-1: all devices)."""
+    lib = load_library()
+    _check(lib, lib.kda_release_workspaces(int(device)))

@@ -1,0 +1,159 @@
+/*
+ * kda.h -- C ABI of the KDA (Kimi Delta Attention) forward-prefill library for
+ * GB300 (sm_103a).
+ *
+ * The operation (per sequence n, head h, token t = 1..L_n):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * with a fp32 state S in R^{128 x 128} per (sequence, head), S_0 = the initial
+ * state (zero when none is given) and final state = S_{L_n}.  It is computed
+ * chunkwise with CHUNK = 16 and D = 128, forward only: a K1 stage prepares the
+ * decayed q/k, applies beta and forms the WY inverse by a 16x16 unit-lower
+ * triangular solve; a K2 stage runs the inter-chunk state recurrence and the
+ * intra-chunk output.  Long sequences may instead run segment-parallel:
+ * K1 -> pre_scan (per-segment summaries) -> merge (carries) -> segment-K2.
+ * Sources: cuLA PR #103 "feat(kda/sm90): FlashKDA prefill port + intracard-CP
+ * prefill" (commit notes: the K1/K2 split, CHUNK=16, D=128, forward only; the
+ * segment pipeline; both states optional), flashinfer PR #4351 "fix(cake_kda):
+ * support non-aligned recurrent prefill head counts" (any positive head count,
+ * H=12 packed varlen, in-place state, atol = rtol = 1e-2 against a reference).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layouts (row-major, contiguous, C order):
+ *   q, k, v, out : bf16 [T_total][H][128]   (dense input [B][T][H][128] is the same memory)
+ *   g            : fp32 [T_total][H][128]   per-token log-decay (not cumulative)
+ *   beta         : bf16 [T_total][H]
+ *   states       : fp32 [N][H][128][128], indexed [n][h][i_k][j_v]
+ *   cu_seqlens   : int32 [N + 1], cu[0] = 0, non-decreasing, cu[N] = T_total
+ * bf16 tensors are passed as uint16_t pointers holding IEEE bfloat16 bits.
+ * Base pointers of q, k, v, g, out, initial_state and final_state must be
+ * 16-byte aligned; beta 2-byte aligned; cu_seqlens 4-byte aligned.
+ *
+ * Ownership: the caller owns every tensor.  The library owns only its
+ * workspaces (device scratch, per device and stream, bounded in number) and
+ * releases them in kda_release_workspaces().  No caller pointer is retained
+ * after a call returns.
+ *
+ * Errors: every entry point returns a kda_status; nothing throws across the
+ * ABI.  Argument validation runs on the host before any launch and has no side
+ * effects when it fails; kda_last_error_message() then says why.  Device-side
+ * conditions (malformed cu_seqlens contents, a bounded wait that ran out) are
+ * recorded in a per-device status word read by kda_get_device_status().
+ *
+ * Asynchrony: kda_prefill / kda_prefill_ex enqueue work on `stream` and return
+ * without synchronising.  `stream` is a cudaStream_t passed as void* (NULL =
+ * the legacy default stream).  The current CUDA device must own all pointers.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1,     /* bad shape, null/misaligned pointer, bad option */
+    KDA_ERR_ALIASING = 2,             /* out overlaps an input; partial state overlap */
+    KDA_ERR_UNSUPPORTED_DEVICE = 3,   /* current device is not compute capability 10.3 */
+    KDA_ERR_OUT_OF_MEMORY = 4,        /* a workspace allocation failed */
+    KDA_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed */
+    KDA_ERR_CAPTURE_NEEDS_WARMUP = 6, /* a workspace would be allocated during stream capture */
+    KDA_ERR_DEVICE_TIMEOUT = 7        /* a device-side bounded wait ran out (status word) */
+} kda_status;
+
+/* Problem shape.  Dense: cu_seqlens == NULL, `batch` sequences of `seq_len`
+ * tokens each (T_total = batch * seq_len, N = batch).  Packed varlen:
+ * cu_seqlens != NULL, batch == 1, seq_len = T_total, num_seqs = N >= 1. */
+typedef struct kda_shape {
+    int32_t batch;
+    int64_t seq_len;
+    int32_t num_seqs;   /* varlen only; ignored for dense input */
+    int32_t num_heads;  /* H >= 1; need not be a multiple of 8 */
+    int32_t head_dim;   /* must be 128 (Dk = Dv = 128) */
+} kda_shape;
+
+/* Execution modes of kda_prefill_ex. */
+#define KDA_MODE_SERIAL 0   /* one fused K1+K2 chain per (sequence, head) */
+#define KDA_MODE_SEGMENT 1  /* segment-parallel: K1 -> pre_scan -> merge -> segment-K2 (dense only) */
+#define KDA_MODE_AUTO 2     /* library picks serial or segment from the shape */
+
+typedef struct kda_options {
+    int32_t mode;         /* KDA_MODE_* (default serial) */
+    int32_t segment_len;  /* segment mode: tokens per segment, multiple of 16; 0 = 8192 */
+    int64_t wait_limit;   /* iteration limit of each device spin wait; 0 = library default */
+} kda_options;
+
+/* kda_prefill -- the forward prefill in serial mode.
+ *   shape          problem shape (host pointer, read during the call only)
+ *   q, k, v, g     device inputs, layouts above; may be NULL only when T_total == 0
+ *   beta           device bf16 [T_total][H]
+ *   scale          output scale (finite), typically 1/sqrt(128)
+ *   initial_state  device fp32 [N][H][128][128] or NULL (= zero state)
+ *   cu_seqlens     device int32 [N + 1] or NULL (dense input)
+ *   out            device bf16 [T_total][H][128]; must not overlap any other argument
+ *   final_state    device fp32 [N][H][128][128] or NULL (not written); may be the
+ *                  very same pointer as initial_state (in-place update) but must not
+ *                  otherwise overlap it or any input
+ *   stream         cudaStream_t (as void*)
+ * A sequence of length 0 writes no output and its final state equals its
+ * initial state.  T_total == 0 with no final state is a no-op returning KDA_OK. */
+kda_status kda_prefill(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
+                       const uint16_t* v, const float* g, const uint16_t* beta, float scale,
+                       const float* initial_state, const int32_t* cu_seqlens, uint16_t* out,
+                       float* final_state, void* stream);
+
+/* kda_prefill_ex -- kda_prefill with options (mode, segment length, wait limit).
+ * opts == NULL behaves as kda_prefill.  Segment mode requires dense input;
+ * segment_len must be a positive multiple of 16. */
+kda_status kda_prefill_ex(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
+                          const uint16_t* v, const float* g, const uint16_t* beta, float scale,
+                          const float* initial_state, const int32_t* cu_seqlens, uint16_t* out,
+                          float* final_state, void* stream, const kda_options* opts);
+
+/* kda_prefill_host -- the same computation on HOST buffers, end to end.
+ * Every tensor pointer (including cu_seqlens) is a host pointer with the
+ * layouts above; page-locked memory gives full copy bandwidth.  The call
+ * copies the inputs into a library-owned device arena on `stream`, runs the
+ * prefill, copies out (and final_state when non-NULL) back, and synchronises
+ * `stream` before returning.  The arena is kept per (device, stream) and
+ * reused; it is freed by kda_release_workspaces(). */
+kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
+                            const uint16_t* v, const float* g, const uint16_t* beta,
+                            float scale, const float* initial_state,
+                            const int32_t* cu_seqlens, uint16_t* out, float* final_state,
+                            void* stream, const kda_options* opts);
+
+/* Bytes of device workspace a call with this shape and these options uses
+ * (0 for serial mode).  No device work; *bytes is written on success. */
+kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, size_t* bytes);
+
+/* Reads and clears the device status word of the current device after
+ * synchronising `stream`.  *code receives KDA_OK, KDA_ERR_INVALID_ARGUMENT
+ * (malformed cu_seqlens contents seen by a kernel) or KDA_ERR_DEVICE_TIMEOUT. */
+kda_status kda_get_device_status(void* stream, int32_t* code);
+
+/* Frees every workspace the library holds on `device` (-1 = all devices).
+ * The caller must ensure no call using them is still running. */
+kda_status kda_release_workspaces(int32_t device);
+
+/* Static description of a status code. */
+const char* kda_status_string(kda_status status);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* kda_last_error_message(void);
+
+/* Library version, e.g. "0.1.0". */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

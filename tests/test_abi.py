@@ -1,0 +1,136 @@
+"""Host-side tests of the C ABI: the library loads, exports every declared symbol,
+and rejects invalid calls with the documented status before any device work."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import chunked_kda_delta_gb300 as K
+from chunked_kda_delta_gb300 import build as kbuild
+from chunked_kda_delta_gb300.kda import KdaOptions, KdaShape
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return K.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    assert set(names) == set(K.kda.EXPORTED_SYMBOLS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_status_strings(lib):
+    for code, name in K.kda._STATUS.items():
+        assert K.kda_status_string(code) == name
+    assert lib.kda_version().decode().count(".") == 2
+
+
+def _call(lib, shape, ptrs=None, scale=0.1, opts=None, **over):
+    # Fake, suitably aligned device-looking addresses: validation never dereferences them.
+    base = dict(q=0x10000000, k=0x20000000, v=0x30000000, g=0x40000000, beta=0x50000000,
+                s0=None, cu=None, out=0x60000000, fin=None)
+    base.update(ptrs or {})
+    base.update(over)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.kda_prefill_ex(ctypes.byref(shape), P(base["q"]), P(base["k"]), P(base["v"]),
+                              P(base["g"]), P(base["beta"]), ctypes.c_float(scale),
+                              P(base["s0"]), P(base["cu"]), P(base["out"]), P(base["fin"]),
+                              None, None if opts is None else ctypes.byref(opts))
+
+
+INVALID, ALIAS = 1, 2
+
+
+@pytest.mark.parametrize("shape", [
+    KdaShape(1, 16, 0, 4, 64),     # head_dim != 128
+    KdaShape(1, 16, 0, 0, 128),    # no heads
+    KdaShape(1, -1, 0, 4, 128),    # negative length
+    KdaShape(0, 16, 0, 4, 128),    # no batch
+])
+def test_bad_shapes_rejected(lib, shape):
+    assert _call(lib, shape) == INVALID
+    assert lib.kda_last_error_message().decode()
+
+
+def test_null_and_misaligned_pointers(lib):
+    s = KdaShape(1, 16, 0, 4, 128)
+    assert _call(lib, s, q=None) == INVALID
+    assert _call(lib, s, out=None) == INVALID
+    assert _call(lib, s, g=0x40000004) == INVALID          # not 16-byte aligned
+    assert _call(lib, s, beta=0x50000001) == INVALID       # odd
+    assert _call(lib, s, s0=0x70000008) == INVALID
+    assert _call(lib, s, scale=float("nan")) == INVALID
+    assert _call(lib, s, scale=float("inf")) == INVALID
+
+
+def test_varlen_rules(lib):
+    assert _call(lib, KdaShape(2, 16, 1, 4, 128), cu=0x70000000) == INVALID  # batch != 1
+    assert _call(lib, KdaShape(1, 16, 0, 4, 128), cu=0x70000000) == INVALID  # num_seqs 0
+    assert _call(lib, KdaShape(1, 16, 1, 4, 128), cu=0x70000002) == INVALID  # misaligned
+    opts = KdaOptions(1, 64, 0)  # segment mode needs dense input
+    assert _call(lib, KdaShape(1, 16, 1, 4, 128), cu=0x70000000, opts=opts) == INVALID
+
+
+def test_options_rules(lib):
+    s = KdaShape(1, 16, 0, 4, 128)
+    assert _call(lib, s, opts=KdaOptions(9, 0, 0)) == INVALID
+    assert _call(lib, s, opts=KdaOptions(1, 24, 0)) == INVALID   # not a multiple of 16
+    assert _call(lib, s, opts=KdaOptions(1, -16, 0)) == INVALID
+    assert _call(lib, s, opts=KdaOptions(0, 0, -1)) == INVALID
+
+
+def test_aliasing_rules(lib):
+    s = KdaShape(1, 16, 0, 4, 128)
+    x = 16 * 4 * 128 * 2
+    # out overlapping q, or sitting inside g
+    assert _call(lib, s, out=0x10000000 + 256) == ALIAS
+    assert _call(lib, s, out=0x40000000 + x) == ALIAS
+    st = 1 * 4 * 128 * 128 * 4
+    # partial overlap of initial and final state is rejected
+    assert _call(lib, s, s0=0x70000000, fin=0x70000000 + 4096) == ALIAS
+    # final state inside an input
+    assert _call(lib, s, fin=0x10000000) == ALIAS
+    # out overlapping the final state
+    assert _call(lib, s, fin=0x70000000, out=0x70000000 + st - 16) == ALIAS
+
+
+def test_in_place_state_passes_validation(lib):
+    s = KdaShape(1, 16, 0, 4, 128)
+    rc = _call(lib, s, s0=0x70000000, fin=0x70000000)
+    # validation accepts the exact alias; without a GPU the next step fails in CUDA
+    assert rc not in (INVALID, ALIAS)
+
+
+def test_workspace_bytes(lib):
+    assert K.kda_workspace_bytes(1, 8192, 64) == 0
+    with pytest.raises(K.KdaError):
+        K.kda_workspace_bytes(1, 8192, 64, head_dim=64)
+
+
+def test_binding_checks_dtypes():
+    q = torch.zeros(16, 2, 128, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        K.kda_prefill_host(q, q, q, q, torch.zeros(16, 2, dtype=torch.bfloat16))
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(K.KdaError):
+        K.load_library(str(tmp_path / "nope.so"))
