@@ -9,6 +9,8 @@
 // bounded (cuLA PR #103, review of the "_get_scratch" cache); an exact alias of
 // the initial and final state is allowed for in-place updates, any partial
 // overlap is rejected (flashinfer PR #4351, review of the overlap checks).
+#include <cudaTypedefs.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -37,7 +39,7 @@ kda_status cuda_fail(cudaError_t e, const char* what) {
 __device__ int32_t g_status_word = 0;
 
 constexpr int kMaxDevices = 64;
-constexpr int64_t kDefaultWaitLimit = 1ll << 26;
+constexpr int64_t kDefaultWaitLimit = 1ll << 22;
 constexpr size_t kMaxWorkspaces = 8;
 
 struct DeviceInfo {
@@ -136,6 +138,46 @@ kda_status get_workspace(int dev, cudaStream_t stream, int kind, size_t bytes, v
     }
     g_workspaces.push_back({dev, (void*)stream, kind, p, bytes, ++g_use_clock});
     *out = p;
+    return KDA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TMA descriptors.  cuTensorMapEncodeTiled is reached through the runtime's
+// driver entry-point query, so the library does not link libcuda directly.
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+kda_status encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        void* f = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
+            return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (%s)",
+                        cudaGetErrorString(e));
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    *fn = g_encode;
+    return KDA_OK;
+}
+
+// [T][H][128] tensor of `elem` bytes per element; box = one 16-row chunk of one head.
+kda_status encode_chunk_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem,
+                            int64_t T, int32_t H, const char* name) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn;
+    kda_status st = encoder(&fn);
+    if (st != KDA_OK) return st;
+    cuuint64_t dims[3] = {(cuuint64_t)kda::kD, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)kda::kD * elem, (cuuint64_t)H * kda::kD * elem};
+    cuuint32_t box[3] = {(cuuint32_t)kda::kD, 1, (cuuint32_t)kda::kChunk};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(KDA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name,
+                    (int)r);
     return KDA_OK;
 }
 
@@ -296,7 +338,16 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
     p.wait_limit = wait_limit;
     p.status = di->status;
     (void)mode;
-    e = kda::launch_serial(p, stream);
+    kda::TensorMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (pr.T_total > 0) {
+        if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "q")) ||
+            (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "k")) ||
+            (st = encode_chunk_map(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "v")) ||
+            (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")))
+            return st;
+    }
+    e = kda::launch_serial(p, maps, stream);
     if (e != cudaSuccess) return cuda_fail(e, "serial prefill launch");
     return KDA_OK;
 }

@@ -2,6 +2,7 @@
 // (host API and kernels).  Not part of the public ABI; see include/kda.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -54,8 +55,14 @@ __device__ __forceinline__ bool seq_range(const FwdParams& p, int n, int64_t& bo
     return true;
 }
 
+// TMA descriptors of the [T_total][H][128] inputs, box {128, 1, 16} (one chunk of
+// one head).  Encoded on the host, passed to kernels as __grid_constant__ params.
+struct TensorMaps {
+    CUtensorMap q, k, v, g;
+};
+
 // Launchers (return the launch error, cudaSuccess on success).
-cudaError_t launch_serial(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream_t stream);
 size_t serial_smem_bytes();
 const void* serial_kernel_symbol();
 

@@ -212,3 +212,17 @@ def test_host_entry_point_matches_device_path():
     o_h, f_h = K.kda_prefill_host(**cpu, scale=inp["scale"],
                                   cu_seqlens=inp["cu_seqlens"].cpu(), output_final_state=True)
     assert torch.equal(o_h, o_dev.cpu()) and torch.equal(f_h, f_dev.cpu())
+
+
+def test_bounded_wait_timeout_is_reported_and_recoverable():
+    """A wait limit of one try_wait round makes waits run out: the kernel must record
+    KDA_ERR_DEVICE_TIMEOUT, drain and exit, leaving the context usable."""
+    inp = make_inputs(custom([2000], 8, True, seed=85), DEV)
+    args = {k: inp[k] for k in ("q", "k", "v", "g", "beta")}
+    K.kda_prefill(**args, scale=inp["scale"], initial_state=inp["initial_state"],
+                  output_final_state=True, wait_limit=1)
+    torch.cuda.synchronize()
+    assert K.kda_get_device_status() == 7
+    out, fin = run_gpu(inp)  # a normal call afterwards still works (and checks status 0)
+    o2, f2 = run_gpu(inp)
+    assert torch.equal(out, o2) and torch.equal(fin, f2)
