@@ -71,6 +71,10 @@ kda_status device_info(int dev, DeviceInfo** out) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kda::serial_smem_bytes())))
             return cuda_fail(e, "cudaFuncSetAttribute(serial kernel)");
+        if ((e = cudaFuncSetAttribute(kda::merge_kernel_symbol(),
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kda::merge_smem_bytes())))
+            return cuda_fail(e, "cudaFuncSetAttribute(merge kernel)");
         d.ready = true;
     }
     *out = &d;
@@ -239,11 +243,16 @@ kda_status validate_shape(const kda_shape* s, bool varlen, Problem* pr) {
 }
 
 kda_status validate_options(const kda_options* o, const Problem& pr, int32_t* mode,
-                            int32_t* seg_len, int64_t* wait_limit) {
+                            int32_t* seg_len, int64_t* wait_limit, int32_t* debug_flags) {
     *mode = KDA_MODE_SERIAL;
     *seg_len = 8192;
     *wait_limit = kDefaultWaitLimit;
+    *debug_flags = 0;
     if (!o) return KDA_OK;
+    if (o->debug_flags & ~KDA_DEBUG_STALL_WAIT)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "unknown debug_flags bits 0x%x", o->debug_flags);
+    if (o->reserved != 0) return fail(KDA_ERR_INVALID_ARGUMENT, "reserved must be 0");
+    *debug_flags = o->debug_flags;
     if (o->mode != KDA_MODE_SERIAL && o->mode != KDA_MODE_SEGMENT && o->mode != KDA_MODE_AUTO)
         return fail(KDA_ERR_INVALID_ARGUMENT, "unknown mode %d", o->mode);
     if (o->segment_len < 0 || (o->segment_len % kda::kChunk) != 0)
@@ -307,11 +316,31 @@ kda_status validate_pointers(const Problem& pr, const uint16_t* q, const uint16_
     return KDA_OK;
 }
 
+// Segment-mode plan: number of segments per sequence and workspace layout
+// (b_seg, m_seg: [B][nseg-1][H][128][128]; carries: [B][nseg][H][128][128], fp32).
+struct SegPlan {
+    int32_t nseg = 0;
+    size_t off_b = 0, off_m = 0, off_c = 0, bytes = 0;
+};
+
+SegPlan plan_segments(const Problem& pr, int32_t seg_len) {
+    SegPlan sp;
+    if (pr.varlen || pr.dense_len <= 0 || seg_len <= 0) return sp;
+    sp.nseg = (int32_t)((pr.dense_len + seg_len - 1) / seg_len);
+    if (sp.nseg <= 1) return sp;
+    const size_t st = (size_t)kda::kD * kda::kD * 4;
+    const size_t per = (size_t)pr.N * pr.H * st;
+    sp.off_b = 0;
+    sp.off_m = per * (sp.nseg - 1);
+    sp.off_c = 2 * per * (sp.nseg - 1);
+    sp.bytes = sp.off_c + per * sp.nseg;
+    return sp;
+}
+
 kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                const float* g, const uint16_t* beta, float scale, const float* s0,
                const int32_t* cu, uint16_t* out, float* sfin, cudaStream_t stream,
-               int32_t mode, int32_t seg_len, int64_t wait_limit) {
-    (void)seg_len;
+               int32_t mode, int32_t seg_len, int64_t wait_limit, int32_t debug_flags) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -336,8 +365,8 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
     p.H = pr.H;
     p.scale = scale;
     p.wait_limit = wait_limit;
+    p.debug_flags = debug_flags;
     p.status = di->status;
-    (void)mode;
     kda::TensorMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (pr.T_total > 0) {
@@ -347,8 +376,43 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
             (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")))
             return st;
     }
-    e = kda::launch_serial(p, maps, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "serial prefill launch");
+    const SegPlan sp = mode == KDA_MODE_SEGMENT ? plan_segments(pr, seg_len) : SegPlan{};
+    if (sp.nseg <= 1) {
+        e = kda::launch_serial(p, maps, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "serial prefill launch");
+        return KDA_OK;
+    }
+    // Segment-parallel: pre_scan (segment summaries from zero and transitions from the
+    // identity, all segments but the last, in parallel) -> merge (carries) -> segment-K2.
+    void* ws = nullptr;
+    if ((st = get_workspace(dev, stream, kWsSegment, sp.bytes, &ws)) != KDA_OK) return st;
+    float* b_seg = reinterpret_cast<float*>(static_cast<char*>(ws) + sp.off_b);
+    float* m_seg = reinterpret_cast<float*>(static_cast<char*>(ws) + sp.off_m);
+    float* carries = reinterpret_cast<float*>(static_cast<char*>(ws) + sp.off_c);
+    kda::FwdParams ps = p;
+    ps.seg_len = seg_len;
+    ps.nseg_total = sp.nseg;
+    ps.nseg_used = sp.nseg - 1;
+    ps.s0 = nullptr;
+    ps.sfin = b_seg;
+    ps.flags = kda::kFlagNoOutput;
+    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
+        return cuda_fail(e, "pre_scan (summary) launch");
+    ps.sfin = m_seg;
+    ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0;
+    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
+        return cuda_fail(e, "pre_scan (transition) launch");
+    if ((e = kda::launch_merge(m_seg, b_seg, s0, carries, pr.N, sp.nseg, pr.H, stream)) !=
+        cudaSuccess)
+        return cuda_fail(e, "merge launch");
+    kda::FwdParams pk = p;
+    pk.seg_len = seg_len;
+    pk.nseg_total = sp.nseg;
+    pk.nseg_used = sp.nseg;
+    pk.s0 = carries;
+    pk.flags = kda::kFlagFinalLastSeg;
+    if ((e = kda::launch_serial(pk, maps, stream)) != cudaSuccess)
+        return cuda_fail(e, "segment-K2 launch");
     return KDA_OK;
 }
 
@@ -364,14 +428,15 @@ kda_status kda_prefill_ex(const kda_shape* shape, const uint16_t* q, const uint1
     Problem pr{};
     kda_status st = validate_shape(shape, cu_seqlens != nullptr, &pr);
     if (st != KDA_OK) return st;
-    int32_t mode, seg_len;
+    int32_t mode, seg_len, debug_flags;
     int64_t wait_limit;
-    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit)) != KDA_OK) return st;
+    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit, &debug_flags)) != KDA_OK)
+        return st;
     if ((st = validate_pointers(pr, q, k, v, g, beta, scale, initial_state, cu_seqlens, out,
                                 final_state)) != KDA_OK)
         return st;
     return run(pr, q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
-               (cudaStream_t)stream, mode, seg_len, wait_limit);
+               (cudaStream_t)stream, mode, seg_len, wait_limit, debug_flags);
 }
 
 kda_status kda_prefill(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
@@ -392,9 +457,10 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
     Problem pr{};
     kda_status st = validate_shape(shape, cu_seqlens != nullptr, &pr);
     if (st != KDA_OK) return st;
-    int32_t mode, seg_len;
+    int32_t mode, seg_len, debug_flags;
     int64_t wait_limit;
-    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit)) != KDA_OK) return st;
+    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit, &debug_flags)) != KDA_OK)
+        return st;
     if (pr.T_total > 0 && (!q || !k || !v || !g || !beta || !out))
         return fail(KDA_ERR_INVALID_ARGUMENT, "a required host pointer is NULL");
     if (pr.varlen) {  // host copy of the offsets: check them here
@@ -441,7 +507,7 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
              reinterpret_cast<uint16_t*>(b + off_b),
              scale, initial_state ? reinterpret_cast<float*>(b + off_s0) : nullptr,
              pr.varlen ? reinterpret_cast<int32_t*>(b + off_cu) : nullptr, d_out, d_fin, stream,
-             mode, seg_len, wait_limit);
+             mode, seg_len, wait_limit, debug_flags);
     if (st != KDA_OK) return st;
     if (x2 && (e = cudaMemcpyAsync(out, d_out, x2, cudaMemcpyDeviceToHost, stream)))
         return cuda_fail(e, "cudaMemcpyAsync device->host (out)");
@@ -457,10 +523,11 @@ kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, 
     Problem pr{};
     kda_status st = validate_shape(shape, false, &pr);
     if (st != KDA_OK) return st;
-    int32_t mode, seg_len;
+    int32_t mode, seg_len, debug_flags;
     int64_t wait_limit;
-    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit)) != KDA_OK) return st;
-    *bytes = 0;
+    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit, &debug_flags)) != KDA_OK)
+        return st;
+    *bytes = mode == KDA_MODE_SEGMENT ? plan_segments(pr, seg_len).bytes : 0;
     return KDA_OK;
 }
 

@@ -16,18 +16,25 @@
 // exp(gam_r - gam_s) is factored through the chunk's row 7 as
 // exp(gam_r - gam_ref) exp(gam_ref - gam_s); each factor stays in fp32 range while
 // the log-decay accumulated over 8 consecutive tokens of a channel is above ~-80.
+// K o exp(gam) and Q o exp(gam) are formed as (K o exp(gam - gam_ref)) exp(gam_ref).
 //
 // Mapping (transposed so the 128-wide value dim is the MMA's M):
 //   TMEM holds S^T (lane j = value column, column i = key row) in fp32.
-//   MMA1: D1[j][0:32]  = S^T[j][:] . [W ; Qtil]^T   (A = bf16 copy of S^T in TMEM,
-//                                                    B = [W ; Qtil] in shared memory)
-//   delta^T = U^T - D1[:, 0:16]   (epilogue threads, written back to TMEM as bf16)
-//   MMA2: S^T += delta^T . Kbar   (after the epilogue scaled S^T by exp(gam_C))
-//   MMA3: D1[:, 16:32] += delta^T . Mq^T;  O^T = scale * D1[:, 16:32]
-// Warp roles (448 threads): warp 0 TMA producer; warp 1 MMA issuer and TMEM owner;
-// warps 2-5 K1 (cumulative decay, decayed operands, in-chunk Grams and the WY
-// solve; the 16x16 products use mma.sync because tcgen05's smallest M is 64);
-// warps 6-13 the K2 epilogue (state conversion/decay, delta, output).
+//   MMA1: P_W = S^T W^T and P_Q = S^T Qtil^T (A = bf16 copy of S^T in TMEM,
+//         B = [W ; Qtil] in shared memory), each as 4 K-quarter partial sums
+//   delta^T = U^T - sum(P_W)   (K2 threads, written back to TMEM as bf16)
+//   MMA2: S^T += delta^T . Kbar   (after the K2 threads scaled S^T by exp(gam_C))
+//   MMA3: P_Q += delta^T . Mq^T;  O^T = scale * sum(P_Q)
+// Warp roles (448 threads): warp 0 TMA producer (and beta, prefetched two chunks
+// ahead); warp 1 TMEM owner; warps 2-5 K1 (cumulative decay, decayed operands,
+// in-chunk Grams and the WY solve; the 16x16 products use mma.sync because tcgen05's
+// smallest M is 64); warps 6-13 K2: state conversion/decay, delta, output, and the
+// tcgen05 MMAs themselves.  The tensor pipe runs the MMAs of one issuing thread one
+// after another but overlaps those of different warps, so each K2 warp issues its own
+// slice: MMA1 is split over the 4 K-quarters into partial accumulators (the warps of
+// one half for S W^T, of the other for S Qtil^T), and the state update into two N=64
+// halves plus Mq delta, issued by three warps.  K2 warps meet at a named barrier
+// instead of handing work to a separate issuing warp.
 // Every wait is bounded: on exhaustion the kernel records KDA_ERR_DEVICE_TIMEOUT
 // in the status word, drains its in-flight copies and MMAs and exits.
 #include <cuda.h>
@@ -46,35 +53,43 @@ constexpr uint32_t kTmemCols = 512;
 // Bound of the waits that drain in-flight copies and MMAs before exit; independent of
 // the caller's wait limit so that an early exit never leaves asynchronous work behind.
 constexpr int64_t kDrainLimit = 1ll << 24;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM column map
 constexpr uint32_t kColS = 0;     // S^T fp32, 128 columns
 constexpr uint32_t kColSA = 128;  // S^T bf16 pairs, 64 columns (MMA1 A operand)
-constexpr uint32_t kColD1 = 192;  // two 32-column buffers (MMA1/MMA3 accumulators)
-constexpr uint32_t kColDA = 256;  // delta^T bf16 pairs, 8 columns (MMA2/MMA3 A operand)
+constexpr uint32_t kColDd = 192;  // 4 partials x 16 columns of S^T W^T
+constexpr uint32_t kColDO = 256;  // 2 buffers x 4 partials x 16 columns of S^T Qtil^T (+ delta^T Mq^T)
+constexpr uint32_t kColDA = 384;  // delta^T bf16 pairs, 8 columns (MMA2/MMA3 A operand)
 
 // Shared memory map (bytes)
-constexpr int kInQ = 0, kInK = 4096, kInV = 8192, kInG = 12288, kInBytes = 20480;
-constexpr uint32_t kTxBytes = kInBytes;
-constexpr int kB1 = 0, kB2 = 8192, kB3 = 12288, kU = 12800, kGC = 20992, kOutBytes = 21504;
+constexpr int kInQ = 0, kInK = 4096, kInV = 8192, kInG = 12288, kInBeta = 20480;
+constexpr int kInBytes = 20608;
+constexpr uint32_t kTxBytes = 20480;  // q, k, v, g tiles
+// U rows are padded to 132 floats so that the fragment-layout float2 stores of the
+// 16x8 MMA tiles (8 rows x 4 lanes) hit 32 distinct banks.
+constexpr int kURow = 132;
+constexpr int kB1 = 0, kB2 = 8192, kB3 = 12288, kU = 12800, kGC = kU + 16 * kURow * 4,
+              kOutBytes = kGC + 512;
 constexpr uint32_t kLbo = 128, kSboB1 = 2048, kSboB2 = 256, kSboB3 = 256;
 constexpr int kStRow = 272, kStArr = 16 * kStRow;  // padded bf16 staging rows (136 elems)
-enum { ST_KQ = 0, ST_QQ, ST_KK, ST_KT, ST_VV, ST_QT, ST_NUM };
+enum { ST_KQ = 0, ST_QQ, ST_KK, ST_VV, ST_NUM };
 constexpr int kSmIn = 0;                               // 2 input stages
 constexpr int kSmOut = kSmIn + 2 * kInBytes;           // 2 K1 output stages
 constexpr int kSmSt = kSmOut + 2 * kOutBytes;          // staging
-constexpr int kSmA = kSmSt + ST_NUM * kStArr;          // fp32 16x16
+constexpr int kSmEref = kSmSt + ST_NUM * kStArr;       // fp32 128: exp(gam_ref)
+constexpr int kSmA = kSmEref + 512;                    // fp32 16x16
 constexpr int kSmTb = kSmA + 1024;                     // bf16 16x24
-constexpr int kSmBeta = kSmTb + 768;                   // fp32 16
+constexpr int kSmBeta = kSmTb + 768;                   // fp32 16 (K1 copy)
 constexpr int kSmBar = kSmBeta + 64;                   // mbarriers
 constexpr int kNumBars = 16;
 constexpr int kSmTmemSlot = kSmBar + kNumBars * 8;
 constexpr int kSmemBytes = kSmTmemSlot + 16;
 enum {
     BAR_IN_FULL = 0, BAR_IN_EMPTY = 2, BAR_K1_FULL = 4, BAR_K1_EMPTY = 6,
-    BAR_SA = 8, BAR_D1 = 9, BAR_DL = 10, BAR_SDONE = 11, BAR_DRAIN = 12
+    BAR_D1 = 8, BAR_SDONE = 9, BAR_DRAIN = 10, BAR_NEVER = 11
 };
-constexpr uint32_t kNamedK1 = 1;
+constexpr uint32_t kNamedK1 = 1, kNamedK2 = 2;
 
 __device__ __forceinline__ uint32_t b1_off(int n, int k) {
     return (n >> 3) * kSboB1 + (k >> 3) * kLbo + (n & 7) * 16 + (k & 7) * 2;
@@ -87,8 +102,31 @@ __device__ __forceinline__ void record(int32_t* status, int32_t code) {
     atomicCAS(status, kStatusOk, code);
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+// C[r][s] = sum_c A[r][c] B[s][c] for 16x16 tiles over 128 channels; A and B are
+// bf16 [16][136] staging arrays.  Four independent accumulator chains.
+__device__ __forceinline__ void gram16(uint32_t abase, uint32_t bbase, int lane, float (&c)[2][4]) {
+    float acc[2][2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
+#pragma unroll
+    for (int k0 = 0; k0 < 128; k0 += 16) {
+        const int kp = (k0 >> 4) & 1;
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        ldsm_x4(abase + (lane & 15) * kStRow + (k0 + 8 * (lane >> 4)) * 2, a0, a1, a2, a3);
+        ldsm_x4(bbase + ((lane & 7) + 8 * (lane >> 4)) * kStRow + (k0 + 8 * ((lane >> 3) & 1)) * 2,
+                b0, b1, b2, b3);
+        mma_16816(acc[kp][0], a0, a1, a2, a3, b0, b1);
+        mma_16816(acc[kp][1], a0, a1, a2, a3, b2, b3);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[j][e] = acc[0][j][e] + acc[1][j][e];
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -113,14 +151,13 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(BAR_IN_FULL + s), 1);
             mbar_init(bar(BAR_IN_EMPTY + s), 1);
-            mbar_init(bar(BAR_K1_FULL + s), 128);
-            mbar_init(bar(BAR_K1_EMPTY + s), 256);
+            mbar_init(bar(BAR_K1_FULL + s), 4);   // one arrival per K1 warp
+            mbar_init(bar(BAR_K1_EMPTY + s), 8);  // one arrival per epilogue warp
         }
-        mbar_init(bar(BAR_SA), 256);
-        mbar_init(bar(BAR_D1), 1);
-        mbar_init(bar(BAR_DL), 256);
-        mbar_init(bar(BAR_SDONE), 1);
-        mbar_init(bar(BAR_DRAIN), 1);
+        mbar_init(bar(BAR_D1), 8);     // one commit per K2 warp (MMA1 slices)
+        mbar_init(bar(BAR_SDONE), 3);  // commits of the two state-update halves and Mq delta
+        mbar_init(bar(BAR_DRAIN), 8);
+        mbar_init(bar(BAR_NEVER), 1);  // never signalled (timeout-path test)
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -140,62 +177,45 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c & 1;
-                if (c >= 2 && !mbar_wait(bar(BAR_IN_EMPTY + s), ((c >> 1) - 1) & 1, lim)) {
-                    record(p.status, kStatusTimeout);
-                    break;
-                }
-                const uint32_t dst = sbase + kSmIn + s * kInBytes;
+        // beta is read with plain loads two chunks ahead (its [T][H] rows are 2 bytes
+        // wide, below the 16-byte TMA granule) and stored next to the TMA tiles.
+        auto load_beta = [&](int cc) -> float {
+            if (lane >= kChunk || cc >= nchunks) return 0.f;
+            const int64_t t = bos + (int64_t)cc * kChunk + lane;
+            return t < eos ? __bfloat162float(p.beta[t * H + h]) : 0.f;
+        };
+        float b_cur = load_beta(0), b_next = load_beta(1);
+        int issued = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c & 1;
+            const bool ok = c < 2 || mbar_wait(bar(BAR_IN_EMPTY + s), ((c >> 1) - 1) & 1, lim);
+            if (__any_sync(0xffffffffu, !ok)) {
+                if (lane == 0) record(p.status, kStatusTimeout);
+                break;
+            }
+            const uint32_t dst = sbase + kSmIn + s * kInBytes;
+            if (lane < kChunk)
+                reinterpret_cast<float*>(smem + kSmIn + s * kInBytes + kInBeta)[lane] = b_cur;
+            b_cur = b_next;
+            b_next = load_beta(c + 2);
+            __syncwarp();
+            if (lane == 0) {
                 const int32_t t0 = (int32_t)(bos + (int64_t)c * kChunk);
                 mbar_arrive_expect_tx(bar(BAR_IN_FULL + s), kTxBytes);
                 tma_load_3d(dst + kInQ, &tm_q, bar(BAR_IN_FULL + s), 0, h, t0);
                 tma_load_3d(dst + kInK, &tm_k, bar(BAR_IN_FULL + s), 0, h, t0);
                 tma_load_3d(dst + kInV, &tm_v, bar(BAR_IN_FULL + s), 0, h, t0);
                 tma_load_3d(dst + kInG, &tm_g, bar(BAR_IN_FULL + s), 0, h, t0);
-                issued = c + 1;
             }
-            // Drain: every issued load must have landed before the CTA exits.
+            issued = c + 1;
+        }
+        // Drain: every issued load must have landed before the CTA exits.
+        if (lane == 0)
             for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c)
                 if (!mbar_wait(bar(BAR_IN_FULL + (c & 1)), (c >> 1) & 1, kDrainLimit))
                     record(p.status, kStatusTimeout);
-        }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc1 = idesc_bf16(128, 32);
-            const uint32_t idesc2 = idesc_bf16(128, 128);
-            const uint32_t idesc3 = idesc_bf16(128, 16);
-            for (int c = 0; c < nchunks; ++c) {
-                const int ks = c & 1;
-                const uint32_t ob = sbase + kSmOut + ks * kOutBytes;
-                if (!mbar_wait(bar(BAR_K1_FULL + ks), (c >> 1) & 1, lim) ||
-                    !mbar_wait(bar(BAR_SA), c & 1, lim)) {
-                    record(p.status, kStatusTimeout);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d1 = tmem + kColD1 + 32u * (uint32_t)(c & 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(d1, tmem + kColSA + 8u * kk, sdesc(ob + kB1 + kk * 2 * kLbo, kLbo, kSboB1),
-                           idesc1, kk > 0);
-                tc_commit(bar(BAR_D1));
-                if (!mbar_wait(bar(BAR_DL), c & 1, lim)) {
-                    record(p.status, kStatusTimeout);
-                    break;
-                }
-                tc_fence_after();
-                mma_ts(tmem + kColS, tmem + kColDA, sdesc(ob + kB2, kLbo, kSboB2), idesc2, 1);
-                mma_ts(d1 + 16, tmem + kColDA, sdesc(ob + kB3, kLbo, kSboB3), idesc3, 1);
-                tc_commit(bar(BAR_SDONE));
-            }
-            // Drain every MMA issued before TMEM is released.
-            tc_commit(bar(BAR_DRAIN));
-            if (!mbar_wait(bar(BAR_DRAIN), 0, kDrainLimit)) record(p.status, kStatusTimeout);
-        }
+        // TMEM owner: allocated above, released after the final barrier.
     } else if (warp < 6) {
         // ------------------------------------------------------------ K1 (128 threads)
         const int kt = tid - 64;          // 0..127
@@ -203,9 +223,13 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int pc = kt & 63;           // channel pair: channels 2pc, 2pc+1
         const int hr = kt >> 6;           // row half: rows 8hr .. 8hr+7
         unsigned char* st = smem + kSmSt;
+        float* eref_sm = reinterpret_cast<float*>(smem + kSmEref);
         float* Asm = reinterpret_cast<float*>(smem + kSmA);
         __nv_bfloat16* Tb = reinterpret_cast<__nv_bfloat16*>(smem + kSmTb);
         float* bet = reinterpret_cast<float*>(smem + kSmBeta);
+        const float2 l2e2 = make_float2(kLog2e, kLog2e), nl2e2 = make_float2(-kLog2e, -kLog2e);
+        const bool zero_v = (p.flags & kFlagZeroV) != 0;
+        const bool with_out = (p.flags & kFlagNoOutput) == 0;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, ks = c & 1;
             bool ok = mbar_wait(bar(BAR_IN_FULL + s), (c >> 1) & 1, lim);
@@ -218,35 +242,30 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int C = (eos - t0 < kChunk) ? (int)(eos - t0) : kChunk;
             const unsigned char* in = smem + kSmIn + s * kInBytes;
             unsigned char* ob = smem + kSmOut + ks * kOutBytes;
-            if (kt < kChunk) bet[kt] = kt < C ? __bfloat162float(p.beta[(t0 + kt) * H + h]) : 0.f;
+            if (kt < kChunk) bet[kt] = reinterpret_cast<const float*>(in + kInBeta)[kt];
 
-            // Phase 1: cumulative decay and decayed operands for channels 2pc, 2pc+1.
+            // Phase 1: cumulative decay (log2 units) and decayed operands for
+            // channels 2pc, 2pc+1, rows 8hr .. 8hr+7.
             const float2* g2 = reinterpret_cast<const float2*>(in + kInG);
-            float ga[kChunk], gb[kChunk];
+            float2 gl[kChunk];
             {
-                float a0 = 0.f, a1 = 0.f;
+                float2 a = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int r = 0; r < kChunk; ++r) {
                     const float2 gv = r < C ? g2[r * 64 + pc] : make_float2(0.f, 0.f);
-                    a0 += gv.x;
-                    a1 += gv.y;
-                    ga[r] = a0;
-                    gb[r] = a1;
+                    a = add2(a, gv);
+                    gl[r] = a;
                 }
             }
-            const float ref0 = ga[kRef], ref1 = gb[kRef];
-            float gh0[8], gh1[8];  // this thread's rows, selected with constant indices
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                gh0[rr] = hr ? ga[8 + rr] : ga[rr];
-                gh1[rr] = hr ? gb[8 + rr] : gb[rr];
-            }
-            const float eref0 = __expf(ref0), eref1 = __expf(ref1);
-            const float ecr0 = __expf(ga[kChunk - 1] - ref0), ecr1 = __expf(gb[kChunk - 1] - ref1);
+            const float2 refl = mul2f(gl[kRef], l2e2);       // gam_ref * log2(e)
+            const float2 nrefl = make_float2(-refl.x, -refl.y);
+            const float2 lastl = mul2f(gl[kChunk - 1], l2e2);
+            const float2 ecr = ex2x2(add2(lastl, nrefl));     // exp(gam_C - gam_ref)
             if (hr == 0) {
-                float* gc = reinterpret_cast<float*>(ob + kGC);
-                gc[2 * pc] = __expf(ga[kChunk - 1]);
-                gc[2 * pc + 1] = __expf(gb[kChunk - 1]);
+                const float2 er = ex2x2(refl);
+                const float2 gc = ex2x2(lastl);
+                reinterpret_cast<float2*>(eref_sm)[pc] = er;
+                reinterpret_cast<float2*>(ob + kGC)[pc] = gc;
             }
             const uint32_t* q2 = reinterpret_cast<const uint32_t*>(in + kInQ);
             const uint32_t* k2 = reinterpret_cast<const uint32_t*>(in + kInK);
@@ -256,26 +275,27 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int rr = 0; rr < 8; ++rr) {
                 const int r = 8 * hr + rr;
                 const bool valid = r < C;
+                const float2 gr = hr ? gl[8 + rr] : gl[rr];
                 const uint32_t qv = valid ? q2[r * 64 + pc] : 0u;
                 const uint32_t kv = valid ? k2[r * 64 + pc] : 0u;
-                const uint32_t vv = valid ? v2[r * 64 + pc] : 0u;
-                const float k0 = bf_lo(kv), k1 = bf_hi(kv), q0 = bf_lo(qv), q1 = bf_hi(qv);
-                const float up0 = __expf(gh0[rr] - ref0), up1 = __expf(gh1[rr] - ref1);
-                const float dn0 = __expf(ref0 - gh0[rr]), dn1 = __expf(ref1 - gh1[rr]);
+                const uint32_t vv = (valid && !zero_v) ? v2[r * 64 + pc] : 0u;
+                const float2 kf = bf2_to_f2(kv), qf = bf2_to_f2(qv);
+                const float2 up = ex2x2(fma2(gr, l2e2, nrefl));   // exp(gam_r - gam_ref)
+                const float2 dn = ex2x2(fma2(gr, nl2e2, refl));   // exp(gam_ref - gam_r)
+                const float2 kq = mul2f(kf, up), qq = mul2f(qf, up), kk = mul2f(kf, dn);
+                const float2 kb = mul2f(kk, ecr);                  // Kbar
                 uint32_t* row = reinterpret_cast<uint32_t*>(st + r * kStRow) + pc;
-                row[ST_KQ * kStArr / 4] = pack_bf16(k0 * up0, k1 * up1);
-                row[ST_QQ * kStArr / 4] = pack_bf16(q0 * up0, q1 * up1);
-                row[ST_KK * kStArr / 4] = pack_bf16(k0 * dn0, k1 * dn1);
-                row[ST_KT * kStArr / 4] = pack_bf16(k0 * up0 * eref0, k1 * up1 * eref1);
-                row[ST_QT * kStArr / 4] = pack_bf16(q0 * up0 * eref0, q1 * up1 * eref1);
+                row[ST_KQ * kStArr / 4] = pack_bf16(kq.x, kq.y);
+                row[ST_QQ * kStArr / 4] = pack_bf16(qq.x, qq.y);
+                row[ST_KK * kStArr / 4] = pack_bf16(kk.x, kk.y);
                 row[ST_VV * kStArr / 4] = vv;
-                const float kbar0 = k0 * dn0 * ecr0, kbar1 = k1 * dn1 * ecr1;
+                const uint32_t w = pack_bf16(kb.x, kb.y);  // lo: channel 2pc, hi: 2pc+1
                 if (rr & 1) {
-                    kb0[rr >> 1] |= pack_bf16(0.f, kbar0) & 0xffff0000u;
-                    kb1[rr >> 1] |= pack_bf16(0.f, kbar1) & 0xffff0000u;
+                    kb0[rr >> 1] |= w << 16;
+                    kb1[rr >> 1] |= w & 0xffff0000u;
                 } else {
-                    kb0[rr >> 1] = pack_bf16(kbar0, 0.f) & 0xffffu;
-                    kb1[rr >> 1] = pack_bf16(kbar1, 0.f) & 0xffffu;
+                    kb0[rr >> 1] = w & 0xffffu;
+                    kb1[rr >> 1] = w >> 16;
                 }
             }
             {   // Kbar rows 2pc, 2pc+1 of B2 (N = key channel, K = chunk row)
@@ -289,22 +309,12 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             named_bar_sync(kNamedK1, 128);
             if (kt == 0) mbar_arrive(bar(BAR_IN_EMPTY + s));  // input tiles consumed
 
-            // Phase 2: in-chunk Grams (warp 0: A and the WY solve; warp 1: Mq),
-            // warps 2-3 move Qtil into rows 16..31 of B1.
-            if (kw < 2) {
-                const uint32_t abase = smem_u32(st + (kw == 0 ? ST_KQ : ST_QQ) * kStArr);
-                const uint32_t bbase = smem_u32(st + ST_KK * kStArr);
-                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                for (int k0 = 0; k0 < 128; k0 += 16) {
-                    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-                    ldsm_x4(abase + (lane & 15) * kStRow + (k0 + 8 * (lane >> 4)) * 2, a0, a1, a2, a3);
-                    ldsm_x4(bbase + ((lane & 7) + 8 * (lane >> 4)) * kStRow +
-                                (k0 + 8 * ((lane >> 3) & 1)) * 2,
-                            b0, b1, b2, b3);
-                    mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                    mma_16816(acc[1], a0, a1, a2, a3, b2, b3);
-                }
+            // Phase 2: warp 0 Gram A and the WY solve; warp 1 Gram Mq; warps 2-3 write
+            // Qtil = (Q o exp(gam - gam_ref)) exp(gam_ref) into rows 16..31 of B1.
+            if (kw == 0 || (kw == 1 && with_out)) {
+                float acc[2][4];
+                gram16(smem_u32(st + (kw == 0 ? ST_KQ : ST_QQ) * kStArr),
+                       smem_u32(st + ST_KK * kStArr), lane, acc);
                 const int g = lane >> 2, t = lane & 3;
                 if (kw == 0) {
 #pragma unroll
@@ -316,15 +326,25 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         }
                     __syncwarp();
                     if (lane < 16) {
+                        // Column sc of T = (I + A)^{-1}: x_r = [r == sc] - sum_{m<r} A[r][m] x_m.
                         const int sc = lane;
                         float x[kChunk];
 #pragma unroll
-                        for (int r = 0; r < kChunk; ++r) x[r] = (r == sc) ? 1.f : 0.f;
+                        for (int r = 0; r < kChunk; ++r) {
+                            float a = 0.f;
+                            const float4* arow = reinterpret_cast<const float4*>(Asm + r * 16);
 #pragma unroll
-                        for (int m = 0; m < kChunk - 1; ++m)
-#pragma unroll
-                            for (int r = m + 1; r < kChunk; ++r)
-                                x[r] = fmaf(-Asm[r * 16 + m], x[m], x[r]);
+                            for (int m4 = 0; m4 < 4; ++m4) {
+                                if (4 * m4 < r) {
+                                    const float4 av = arow[m4];
+                                    if (4 * m4 + 0 < r) a = fmaf(av.x, x[4 * m4 + 0], a);
+                                    if (4 * m4 + 1 < r) a = fmaf(av.y, x[4 * m4 + 1], a);
+                                    if (4 * m4 + 2 < r) a = fmaf(av.z, x[4 * m4 + 2], a);
+                                    if (4 * m4 + 3 < r) a = fmaf(av.w, x[4 * m4 + 3], a);
+                                }
+                            }
+                            x[r] = r < sc ? 0.f : (r == sc ? 1.f : -a);
+                        }
                         const float bs = bet[sc];
 #pragma unroll
                         for (int r = 0; r < kChunk; ++r) Tb[r * 24 + sc] = __float2bfloat16_rn(x[r] * bs);
@@ -341,19 +361,28 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             *reinterpret_cast<uint32_t*>(b3 + b3_off(r, sc)) = pack_bf16(m0, m1);
                         }
                 }
-            } else {
+            } else if (kw >= 2 && with_out) {
                 const int ct = kt - 64;  // 0..63
                 unsigned char* b1 = ob + kB1;
 #pragma unroll
                 for (int e = ct; e < 256; e += 64) {
-                    const int r = e >> 4, kg = e & 15;
+                    const int r = e & 15, kg = e >> 4;  // 8 consecutive rows per 128-byte store
+                    const uint4 src = *reinterpret_cast<const uint4*>(st + ST_QQ * kStArr + r * kStRow + kg * 16);
+                    const float4 e0 = reinterpret_cast<const float4*>(eref_sm)[2 * kg];
+                    const float4 e1 = reinterpret_cast<const float4*>(eref_sm)[2 * kg + 1];
+                    const float2 x0 = mul2f(bf2_to_f2(src.x), make_float2(e0.x, e0.y));
+                    const float2 x1 = mul2f(bf2_to_f2(src.y), make_float2(e0.z, e0.w));
+                    const float2 x2 = mul2f(bf2_to_f2(src.z), make_float2(e1.x, e1.y));
+                    const float2 x3 = mul2f(bf2_to_f2(src.w), make_float2(e1.z, e1.w));
                     *reinterpret_cast<uint4*>(b1 + b1_off(16 + r, kg * 8)) =
-                        *reinterpret_cast<const uint4*>(st + ST_QT * kStArr + r * kStRow + kg * 16);
+                        make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x1.x, x1.y),
+                                   pack_bf16(x2.x, x2.y), pack_bf16(x3.x, x3.y));
                 }
             }
             named_bar_sync(kNamedK1, 128);
 
-            // Phase 3: W = Tb Ktil, U = Tb V; K1 warp kw owns columns [32kw, 32kw + 32).
+            // Phase 3: W = (Tb (K o exp(gam - gam_ref))) o exp(gam_ref), U = Tb V;
+            // K1 warp kw owns columns [32kw, 32kw + 32).
             {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(smem_u32(Tb) + (lane & 15) * 48 + 8 * (lane >> 4) * 2, a0, a1, a2, a3);
@@ -362,7 +391,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 float* U = reinterpret_cast<float*>(ob + kU);
 #pragma unroll
                 for (int which = 0; which < 2; ++which) {
-                    const uint32_t bb = smem_u32(st + (which == 0 ? ST_KT : ST_VV) * kStArr);
+                    const uint32_t bb = smem_u32(st + (which == 0 ? ST_KQ : ST_VV) * kStArr);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int n0 = 32 * kw + 16 * half;
@@ -378,45 +407,98 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             const float* d = nt ? d1 : d0;
                             const int col = n0 + 8 * nt + 2 * t;
                             if (which == 0) {
-                                *reinterpret_cast<uint32_t*>(b1 + b1_off(g, col)) = pack_bf16(d[0], d[1]);
-                                *reinterpret_cast<uint32_t*>(b1 + b1_off(g + 8, col)) = pack_bf16(d[2], d[3]);
+                                const float2 er = reinterpret_cast<const float2*>(eref_sm)[col >> 1];
+                                const float2 w0 = mul2f(make_float2(d[0], d[1]), er);
+                                const float2 w1 = mul2f(make_float2(d[2], d[3]), er);
+                                *reinterpret_cast<uint32_t*>(b1 + b1_off(g, col)) = pack_bf16(w0.x, w0.y);
+                                *reinterpret_cast<uint32_t*>(b1 + b1_off(g + 8, col)) = pack_bf16(w1.x, w1.y);
                             } else {
-                                *reinterpret_cast<float2*>(U + g * 128 + col) = make_float2(d[0], d[1]);
-                                *reinterpret_cast<float2*>(U + (g + 8) * 128 + col) = make_float2(d[2], d[3]);
+                                *reinterpret_cast<float2*>(U + g * kURow + col) = make_float2(d[0], d[1]);
+                                *reinterpret_cast<float2*>(U + (g + 8) * kURow + col) = make_float2(d[2], d[3]);
                             }
                         }
                     }
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(bar(BAR_K1_FULL + ks));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_K1_FULL + ks));
         }
     } else {
-        // ------------------------------------------------------------ K2 epilogue (256 threads)
-        const int quad = warp & 3;
+        // ------------------------------------------------------------ K2 (256 threads)
+        const int quad = warp & 3;                 // TMEM lane quadrant = SM sub-partition
         const int hf = (warp - 6) >> 2;            // 0: key columns 0-63, 1: 64-127
         const int j = 32 * quad + lane;            // value column owned by this thread
         const uint32_t lanes = (uint32_t)(32 * quad) << 16;
         const uint32_t tS = tmem + lanes + kColS + 64u * hf;
         const uint32_t tSA = tmem + lanes + kColSA + 32u * hf;
         const uint32_t tDA = tmem + lanes + kColDA + 4u * hf;
+        const uint32_t idesc16 = idesc_bf16(128, 16), idesc64 = idesc_bf16(128, 64);
+        const bool with_out = (p.flags & kFlagNoOutput) == 0;
+        // State rows: initial state at this CTA's row; final state at its row, or (segment
+        // runs) at sequence b for the last segment only.
         const size_t soff = ((size_t)n * p.H + h) * kD * kD;
+        size_t foff = soff;
+        bool write_final = p.sfin != nullptr;
+        if (p.flags & kFlagFinalLastSeg) {
+            const int b = n / p.nseg_used, sg = n % p.nseg_used;
+            write_final = write_final && sg == p.nseg_total - 1;
+            foff = ((size_t)b * p.H + h) * kD * kD;
+        }
         uint32_t sreg[64];
         // Initial state S0[i][j] for keys i of this half -> S^T[j][i].
+        if (p.flags & kFlagIdentityS0) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-            sreg[i] = p.s0 ? __float_as_uint(p.s0[soff + (size_t)(64 * hf + i) * kD + j]) : 0u;
+            for (int i = 0; i < 64; ++i) sreg[i] = (64 * hf + i == j) ? __float_as_uint(1.f) : 0u;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                sreg[i] = p.s0 ? __float_as_uint(p.s0[soff + (size_t)(64 * hf + i) * kD + j]) : 0u;
+        }
         tmem_st32(tS, sreg);
         tmem_st32(tS + 32, sreg + 32);
         tmem_wait_st();
-        bool ok = true;
-        int c = 0;
-        for (; c < nchunks; ++c) {
-            const int ks = c & 1;
-            if (c > 0) {
-                if (!mbar_wait(bar(BAR_SDONE), (c - 1) & 1, lim)) { ok = false; break; }
-                tc_fence_after();
+        // Sum over the 4 K-quarter partials of 8 accumulator columns (rows 8hf..8hf+7).
+        auto ld_partials = [&](uint32_t col0, float (&v)[8]) {
+            uint32_t a[8], b[8], c2[8], d[8];
+            tmem_ld8(tmem + lanes + col0 + 8 * hf, a);
+            tmem_ld8(tmem + lanes + col0 + 16 + 8 * hf, b);
+            tmem_ld8(tmem + lanes + col0 + 32 + 8 * hf, c2);
+            tmem_ld8(tmem + lanes + col0 + 48 + 8 * hf, d);
+            tmem_wait_ld_regs<8>(a);
+            tmem_wait_ld_regs<8>(b);
+            tmem_wait_ld_regs<8>(c2);
+            tmem_wait_ld_regs<8>(d);
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                v[r] = (__uint_as_float(a[r]) + __uint_as_float(b[r])) +
+                       (__uint_as_float(c2[r]) + __uint_as_float(d[r]));
+        };
+        auto store_out = [&](int cp) {
+            const int64_t t0p = bos + (int64_t)cp * kChunk;
+            const int Cp = (eos - t0p < kChunk) ? (int)(eos - t0p) : kChunk;
+            float o[8];
+            ld_partials(kColDO + 64u * (cp & 1), o);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int row = 8 * hf + r;
+                if (row < Cp)
+                    p.out[((t0p + row) * H + h) * kD + j] = __float2bfloat16_rn(p.scale * o[r]);
             }
+        };
+        bool ok = true;
+        if (p.debug_flags & 1) ok = mbar_wait(bar(BAR_NEVER), 0, lim);  // nothing signals it
+        if (named_bar_or(kNamedK2, 256, !ok)) ok = false;
+        for (int c = 0; ok && c < nchunks; ++c) {
+            const int ks = c & 1;
+            const uint32_t ob = sbase + kSmOut + ks * kOutBytes;
+            bool w = mbar_wait(bar(BAR_K1_FULL + ks), (c >> 1) & 1, lim);
+            if (c > 0) w = w && mbar_wait(bar(BAR_SDONE), (c - 1) & 1, lim);
+            if (named_bar_or(kNamedK2, 256, !w)) { ok = false; break; }
+            tc_fence_after();
+            // The previous chunk's K1 stage is no longer read (its U and exp(gam_C) were
+            // consumed last iteration; the MMAs reading B1..B3 completed).
+            if (c > 0 && lane == 0) mbar_arrive(bar(BAR_K1_EMPTY + ((c - 1) & 1)));
             // (A) S_c (this half) -> bf16 copy for MMA1
             tmem_ld32(tS, sreg);
             tmem_ld32(tS + 32, sreg + 32);
@@ -430,29 +512,30 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_wait_st();
             }
             tc_fence_before();
-            mbar_arrive(bar(BAR_SA));
-            // (C) output rows of the previous chunk, then release its K1 stage
-            if (c > 0) {
-                const int cp = c - 1;
-                const int64_t t0p = bos + (int64_t)cp * kChunk;
-                const int Cp = (eos - t0p < kChunk) ? (int)(eos - t0p) : kChunk;
-                uint32_t o[8];
-                tmem_ld8(tmem + lanes + kColD1 + 32u * (cp & 1) + 16 + 8 * hf, o);
-                tmem_wait_ld_regs<8>(o);
+            named_bar_sync(kNamedK2, 256);
+            tc_fence_after();
+            // MMA1 slice of this warp: K-quarter `quad`; half 0 -> S^T W^T partial,
+            // half 1 -> S^T Qtil^T partial (not needed without output rows).
+            if (elect_one()) {
+              if (hf == 0 || with_out) {
+                const uint32_t bb = ob + kB1 + (uint32_t)hf * 2u * kSboB1;
+                const uint32_t d = hf == 0 ? tmem + kColDd + 16u * quad
+                                           : tmem + kColDO + 64u * (c & 1) + 16u * quad;
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int row = 8 * hf + r;
-                    if (row < Cp)
-                        p.out[((t0p + row) * H + h) * kD + j] =
-                            __float2bfloat16_rn(p.scale * __uint_as_float(o[r]));
+                for (int s2 = 0; s2 < 2; ++s2) {
+                    const int kk = 2 * quad + s2;
+                    mma_ts(d, tmem + kColSA + 8u * kk, sdesc(bb + kk * 2 * kLbo, kLbo, kSboB1),
+                           idesc16, s2);
                 }
-                mbar_arrive(bar(BAR_K1_EMPTY + (cp & 1)));
+              }
+                tc_commit(bar(BAR_D1));
             }
-            // (D) decay S by exp(gam_C) ahead of MMA2
-            if (!mbar_wait(bar(BAR_K1_FULL + ks), (c >> 1) & 1, lim)) { ok = false; break; }
-            const unsigned char* ob = smem + kSmOut + ks * kOutBytes;
+            __syncwarp();
+            // (C) output rows of the previous chunk
+            if (c > 0 && with_out) store_out(c - 1);
+            // (D) decay S by exp(gam_C) ahead of the state update
             {
-                const float4* gc4 = reinterpret_cast<const float4*>(ob + kGC) + 16 * hf;
+                const float4* gc4 = reinterpret_cast<const float4*>(smem + kSmOut + ks * kOutBytes + kGC) + 16 * hf;
 #pragma unroll
                 for (int i4 = 0; i4 < 16; ++i4) {
                     const float4 gv = gc4[i4];
@@ -469,60 +552,64 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_st32(tS + 32, sreg + 32);
             }
             // (B) delta^T = U^T - (S^T W^T) for rows 8hf .. 8hf+7
-            if (!mbar_wait(bar(BAR_D1), c & 1, lim)) { ok = false; break; }
-            tc_fence_after();
-            {
-                uint32_t d[8];
-                tmem_ld8(tmem + lanes + kColD1 + 32u * (c & 1) + 8 * hf, d);
-                tmem_wait_ld_regs<8>(d);
-                const float* U = reinterpret_cast<const float*>(ob + kU);
+            w = mbar_wait(bar(BAR_D1), c & 1, lim);
+            if (w) {
+                tc_fence_after();
+                float dsum[8];
+                ld_partials(kColDd, dsum);
+                const float* U = reinterpret_cast<const float*>(smem + kSmOut + ks * kOutBytes + kU);
                 uint32_t pk[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int r0 = 8 * hf + 2 * r;
-                    const float d0 = U[r0 * 128 + j] - __uint_as_float(d[2 * r]);
-                    const float d1 = U[(r0 + 1) * 128 + j] - __uint_as_float(d[2 * r + 1]);
-                    pk[r] = pack_bf16(d0, d1);
+                    pk[r] = pack_bf16(U[r0 * kURow + j] - dsum[2 * r], U[(r0 + 1) * kURow + j] - dsum[2 * r + 1]);
                 }
                 tmem_st4(tDA, pk);
-                tmem_wait_st();
             }
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(BAR_DL));
+            if (named_bar_or(kNamedK2, 256, !w)) { ok = false; break; }
+            tc_fence_after();
+            // State update (two N=64 halves) and Mq delta into the first O partial.
+            if (hf == 0 && quad < 3) {
+                if (elect_one()) {
+                    if (quad < 2)
+                        mma_ts(tmem + kColS + 64u * quad, tmem + kColDA,
+                               sdesc(ob + kB2 + quad * 8 * kSboB2, kLbo, kSboB2), idesc64, 1);
+                    else if (with_out)
+                        mma_ts(tmem + kColDO + 64u * (c & 1), tmem + kColDA,
+                               sdesc(ob + kB3, kLbo, kSboB3), idesc16, 1);
+                    tc_commit(bar(BAR_SDONE));
+                }
+                __syncwarp();
+            }
         }
         if (ok && nchunks > 0) {
             // Output of the last chunk and the final state.
-            if (!mbar_wait(bar(BAR_SDONE), (nchunks - 1) & 1, lim)) {
+            const bool w = mbar_wait(bar(BAR_SDONE), (nchunks - 1) & 1, lim);
+            if (named_bar_or(kNamedK2, 256, !w)) {
                 ok = false;
             } else {
                 tc_fence_after();
-                const int cp = nchunks - 1;
-                const int64_t t0p = bos + (int64_t)cp * kChunk;
-                const int Cp = (eos - t0p < kChunk) ? (int)(eos - t0p) : kChunk;
-                uint32_t o[8];
-                tmem_ld8(tmem + lanes + kColD1 + 32u * (cp & 1) + 16 + 8 * hf, o);
-                tmem_wait_ld_regs<8>(o);
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int row = 8 * hf + r;
-                    if (row < Cp)
-                        p.out[((t0p + row) * H + h) * kD + j] =
-                            __float2bfloat16_rn(p.scale * __uint_as_float(o[r]));
-                }
+                if (with_out) store_out(nchunks - 1);
             }
         }
         if (!ok) {
-            record(p.status, kStatusTimeout);
+            if (lane == 0) record(p.status, kStatusTimeout);
             tmem_wait_st();
             tmem_wait_ld();
-        } else if (p.sfin) {
+        } else if (write_final) {
             tmem_ld32(tS, sreg);
             tmem_ld32(tS + 32, sreg + 32);
             tmem_wait_ld_regs<64>(sreg);
 #pragma unroll
             for (int i = 0; i < 64; ++i)
-                p.sfin[soff + (size_t)(64 * hf + i) * kD + j] = __uint_as_float(sreg[i]);
+                p.sfin[foff + (size_t)(64 * hf + i) * kD + j] = __uint_as_float(sreg[i]);
         }
+        // Drain every MMA this warp issued before TMEM is released.
+        if (elect_one()) tc_commit(bar(BAR_DRAIN));
+        __syncwarp();
+        if (!mbar_wait(bar(BAR_DRAIN), 0, kDrainLimit) && lane == 0) record(p.status, kStatusTimeout);
     }
 
     tc_fence_before();
@@ -539,7 +626,8 @@ size_t serial_smem_bytes() { return kSmemBytes; }
 const void* serial_kernel_symbol() { return reinterpret_cast<const void*>(&kda_fwd_tc_kernel); }
 
 cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream_t stream) {
-    const long long blocks = (long long)p.N * p.H;
+    const long long rows = p.seg_len > 0 ? (long long)p.N * p.nseg_used : (long long)p.N;
+    const long long blocks = rows * p.H;
     if (blocks == 0) return cudaSuccess;
     kda_fwd_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(maps.q, maps.k, maps.v,
                                                                           maps.g, p);

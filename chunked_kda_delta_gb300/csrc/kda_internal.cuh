@@ -34,13 +34,34 @@ struct FwdParams {
     int32_t H;
     float scale;
     int64_t wait_limit;   // iteration limit of bounded spin waits
+    int32_t debug_flags;  // KDA_DEBUG_* bits (failure-path tests only)
     int32_t* status;      // device status word of this device
+    // Segment launches (seg_len > 0): CTA row n' = b * nseg_used + s runs segment s of
+    // dense sequence b, tokens [b*L + s*seg_len, b*L + min((s+1)*seg_len, L)), L = dense_len.
+    int64_t seg_len;
+    int32_t nseg_used;    // segments of each sequence covered by this launch
+    int32_t nseg_total;   // segments of each sequence
+    int32_t flags;        // kFlag* below
 };
+
+// Launch flags of the fused kernel.
+constexpr int32_t kFlagNoOutput = 1;       // no output rows (summary runs)
+constexpr int32_t kFlagZeroV = 2;          // treat v as zero (transition runs: U = 0)
+constexpr int32_t kFlagIdentityS0 = 4;     // initial state = identity
+constexpr int32_t kFlagFinalLastSeg = 8;   // write final state only for the last segment, at index b
 
 // Token range [bos, eos) of sequence n; false (and the status word set) when
 // cu_seqlens is malformed for this sequence.
 __device__ __forceinline__ bool seq_range(const FwdParams& p, int n, int64_t& bos,
                                           int64_t& eos) {
+    if (p.seg_len > 0) {
+        const int b = n / p.nseg_used, sg = n % p.nseg_used;
+        const int64_t base = (int64_t)b * p.dense_len;
+        const int64_t a = (int64_t)sg * p.seg_len;
+        bos = base + a;
+        eos = base + (a + p.seg_len < p.dense_len ? a + p.seg_len : p.dense_len);
+        return true;
+    }
     if (p.cu == nullptr) {
         bos = (int64_t)n * p.dense_len;
         eos = bos + p.dense_len;
@@ -62,8 +83,14 @@ struct TensorMaps {
 };
 
 // Launchers (return the launch error, cudaSuccess on success).
+// Fused K1+K2 kernel over p.N x p.H rows (or the segment rows of a segment launch).
 cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream_t stream);
+// Segment merge: carry[b][0] = S0[b] (or 0), carry[b][s+1] = m[b][s] carry[b][s] + bs[b][s].
+cudaError_t launch_merge(const float* m_seg, const float* b_seg, const float* s0, float* carries,
+                         int32_t B, int32_t nseg, int32_t H, cudaStream_t stream);
 size_t serial_smem_bytes();
 const void* serial_kernel_symbol();
+size_t merge_smem_bytes();
+const void* merge_kernel_symbol();
 
 }  // namespace kda

@@ -49,7 +49,8 @@ class KdaShape(ctypes.Structure):
 
 class KdaOptions(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("segment_len", ctypes.c_int32),
-                ("wait_limit", ctypes.c_int64)]
+                ("wait_limit", ctypes.c_int64), ("debug_flags", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -147,8 +148,11 @@ def _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, device_type):
             raise ValueError(f"cu_seqlens must be on {device_type}")
 
 
-def _options(mode, segment_len, wait_limit):
-    return KdaOptions(int(mode), int(segment_len), int(wait_limit))
+DEBUG_STALL_WAIT = 1
+
+
+def _options(mode, segment_len, wait_limit, debug_flags=0):
+    return KdaOptions(int(mode), int(segment_len), int(wait_limit), int(debug_flags), 0)
 
 
 def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
@@ -158,7 +162,8 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
                 out: Optional[torch.Tensor] = None,
                 final_state: Optional[torch.Tensor] = None,
                 stream=None, output_final_state: bool = False,
-                mode: int = MODE_SERIAL, segment_len: int = 0, wait_limit: int = 0):
+                mode: int = MODE_SERIAL, segment_len: int = 0, wait_limit: int = 0,
+                debug_flags: int = 0):
     """KDA forward prefill on CUDA tensors; returns ``(out, final_state)``.
 
     q, k, v: bf16 ``[T, H, 128]`` (or ``[B, T, H, 128]`` dense); g: fp32 of the
@@ -184,7 +189,7 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif isinstance(stream, torch.cuda.Stream):
         stream = stream.cuda_stream
-    opts = _options(mode, segment_len, wait_limit)
+    opts = _options(mode, segment_len, wait_limit, debug_flags)
     with torch.cuda.device(q.device):
         st = lib.kda_prefill_ex(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                 _ptr(beta), ctypes.c_float(scale), _ptr(initial_state),

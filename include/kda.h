@@ -88,7 +88,15 @@ typedef struct kda_options {
     int32_t mode;         /* KDA_MODE_* (default serial) */
     int32_t segment_len;  /* segment mode: tokens per segment, multiple of 16; 0 = 8192 */
     int64_t wait_limit;   /* iteration limit of each device spin wait; 0 = library default */
+    int32_t debug_flags;  /* 0 in normal use; KDA_DEBUG_* bits for failure-path tests */
+    int32_t reserved;     /* must be 0 */
 } kda_options;
+
+/* debug_flags bit: the kernel's first state-pipeline wait is on a barrier that nothing
+ * signals, so its bounded wait runs out; the call then records KDA_ERR_DEVICE_TIMEOUT in
+ * the device status word, drains its in-flight copies and returns with garbage outputs.
+ * Exists to test the timeout path without faulting or hanging the GPU. */
+#define KDA_DEBUG_STALL_WAIT 1
 
 /* kda_prefill -- the forward prefill in serial mode.
  *   shape          problem shape (host pointer, read during the call only)

@@ -85,16 +85,18 @@ def test_varlen_rules(lib):
     assert _call(lib, KdaShape(2, 16, 1, 4, 128), cu=0x70000000) == INVALID  # batch != 1
     assert _call(lib, KdaShape(1, 16, 0, 4, 128), cu=0x70000000) == INVALID  # num_seqs 0
     assert _call(lib, KdaShape(1, 16, 1, 4, 128), cu=0x70000002) == INVALID  # misaligned
-    opts = KdaOptions(1, 64, 0)  # segment mode needs dense input
+    opts = KdaOptions(1, 64, 0, 0, 0)  # segment mode needs dense input
     assert _call(lib, KdaShape(1, 16, 1, 4, 128), cu=0x70000000, opts=opts) == INVALID
 
 
 def test_options_rules(lib):
     s = KdaShape(1, 16, 0, 4, 128)
-    assert _call(lib, s, opts=KdaOptions(9, 0, 0)) == INVALID
-    assert _call(lib, s, opts=KdaOptions(1, 24, 0)) == INVALID   # not a multiple of 16
-    assert _call(lib, s, opts=KdaOptions(1, -16, 0)) == INVALID
-    assert _call(lib, s, opts=KdaOptions(0, 0, -1)) == INVALID
+    assert _call(lib, s, opts=KdaOptions(9, 0, 0, 0, 0)) == INVALID
+    assert _call(lib, s, opts=KdaOptions(1, 24, 0, 0, 0)) == INVALID   # not a multiple of 16
+    assert _call(lib, s, opts=KdaOptions(1, -16, 0, 0, 0)) == INVALID
+    assert _call(lib, s, opts=KdaOptions(0, 0, -1, 0, 0)) == INVALID
+    assert _call(lib, s, opts=KdaOptions(0, 0, 0, 2, 0)) == INVALID    # unknown debug bit
+    assert _call(lib, s, opts=KdaOptions(0, 0, 0, 0, 1)) == INVALID    # reserved != 0
 
 
 def test_aliasing_rules(lib):

@@ -215,14 +215,16 @@ def test_host_entry_point_matches_device_path():
 
 
 def test_bounded_wait_timeout_is_reported_and_recoverable():
-    """A wait limit of one try_wait round makes waits run out: the kernel must record
-    KDA_ERR_DEVICE_TIMEOUT, drain and exit, leaving the context usable."""
+    """With the stall flag the kernel waits on a barrier nothing signals: its bounded
+    wait must run out, KDA_ERR_DEVICE_TIMEOUT is recorded, copies and MMAs drain, the
+    kernel exits, and the context stays usable for the next call."""
     inp = make_inputs(custom([2000], 8, True, seed=85), DEV)
     args = {k: inp[k] for k in ("q", "k", "v", "g", "beta")}
     K.kda_prefill(**args, scale=inp["scale"], initial_state=inp["initial_state"],
-                  output_final_state=True, wait_limit=1)
+                  output_final_state=True, wait_limit=2000, debug_flags=K.kda.DEBUG_STALL_WAIT)
     torch.cuda.synchronize()
     assert K.kda_get_device_status() == 7
+    assert K.kda_get_device_status() == 0
     out, fin = run_gpu(inp)  # a normal call afterwards still works (and checks status 0)
     o2, f2 = run_gpu(inp)
     assert torch.equal(out, o2) and torch.equal(fin, f2)

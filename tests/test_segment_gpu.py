@@ -1,0 +1,114 @@
+"""Segment-parallel prefill (pre_scan -> merge -> segment-K2) on the GPU.
+
+The pages claim the segment pipeline is bit-identical to the serial one (cuLA PR #103
+commit notes and test list: "CP vs serial bit-exactness (torch.equal)").  Under the
+plain reading of the pipeline the carries are products of per-segment transitions and
+round differently from the serial chain, so this suite requires both modes to match
+the fp64 oracle within atol = rtol = 1e-2 and reports the max abs difference between
+them instead of asserting equality.
+"""
+import pytest
+import torch
+
+import chunked_kda_delta_gb300 as K
+from chunked_kda_delta_gb300 import build as kbuild
+from chunked_kda_delta_gb300.inputs import WORKLOADS, custom, make_inputs, to_f64_numpy
+
+from kda_testutil import assert_close, gpu_out_heads, gpu_state_heads, oracle_on_heads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kbuild.build()
+    K.load_library()
+
+
+def run(inp, mode, seg_len=0, stream=None):
+    w = inp["workload"]
+    B, T = w.num_seqs, w.seq_lens[0]
+    q, k, v, g = (inp[x].view(B, T, w.num_heads, 128) for x in ("q", "k", "v", "g"))
+    beta = inp["beta"].view(B, T, w.num_heads)
+    out, fin = K.kda_prefill(q, k, v, g, beta, inp["scale"], initial_state=inp["initial_state"],
+                             output_final_state=True, mode=mode, segment_len=seg_len,
+                             stream=stream)
+    torch.cuda.synchronize()
+    assert K.kda_get_device_status() == 0
+    return out.reshape(-1, w.num_heads, 128), fin
+
+
+@pytest.mark.parametrize("B,T,seg,with_s0", [
+    (1, 200, 64, True),     # 4 segments, ragged last one (8 tokens)
+    (2, 130, 32, True),     # dense batch, 5 segments, ragged last chunk inside a segment
+    (1, 256, 64, False),    # segments divide T
+    (3, 48, 16, True),      # one chunk per segment
+    (1, 40, 64, True),      # a single segment: plain serial path
+])
+def test_segment_matches_oracle(orc, B, T, seg, with_s0):
+    inp = make_inputs(custom([T] * B, 4, with_s0, seed=300 + T + seg), DEV)
+    out, fin = run(inp, K.MODE_SEGMENT, seg)
+    o_ref, f_ref = oracle_on_heads(orc, inp, range(4))
+    assert_close(gpu_out_heads(out, range(4)), o_ref, "segment out")
+    assert_close(gpu_state_heads(fin, range(4)), f_ref, "segment final")
+
+
+def test_segment_stress_slow_decay(orc):
+    """Slow decay makes a wrong carry or transition visible far downstream."""
+    inp = make_inputs(custom([512], 4, True, seed=310), DEV, stress=True)
+    out, fin = run(inp, K.MODE_SEGMENT, 128)
+    o_ref, f_ref = oracle_on_heads(orc, inp, range(4))
+    assert_close(gpu_out_heads(out, range(4)), o_ref, "segment stress out")
+    assert_close(gpu_state_heads(fin, range(4)), f_ref, "segment stress final")
+
+
+def test_segment_vs_serial_long_workload(orc):
+    """T = 131072, H = 64, segments of 8192 tokens: both modes against the oracle on
+    sampled heads, and the max abs difference between the two modes over every output."""
+    inp = make_inputs(WORKLOADS["long_t131072_h64"], DEV)
+    o_ser, f_ser = run(inp, K.MODE_SERIAL)
+    o_seg, f_seg = run(inp, K.MODE_SEGMENT, 8192)
+    heads = [0, 63]
+    o_ref, f_ref = oracle_on_heads(orc, inp, heads)
+    assert_close(gpu_out_heads(o_seg, heads), o_ref, "segment out (sampled heads)")
+    assert_close(gpu_state_heads(f_seg, heads), f_ref, "segment final (sampled heads)")
+    d_out = (o_seg.float() - o_ser.float()).abs().max().item()
+    d_fin = (f_seg - f_ser).abs().max().item()
+    print(f"\nsegment vs serial max |diff|: out {d_out:.3e}, final state {d_fin:.3e}")
+    assert d_out < 2e-2 and d_fin < 2e-2
+
+
+def test_workspace_bytes_matches_plan():
+    nb = K.kda_workspace_bytes(1, 131072, 64, mode=K.MODE_SEGMENT, segment_len=8192)
+    assert nb == (2 * 15 + 16) * 64 * 128 * 128 * 4
+    assert K.kda_workspace_bytes(1, 8192, 64, mode=K.MODE_SEGMENT, segment_len=8192) == 0
+
+
+def test_capture_without_warmup_is_refused():
+    inp = make_inputs(custom([256], 2, False, seed=311), DEV)
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with pytest.raises(K.KdaError) as ei:
+        with torch.cuda.graph(graph, stream=s):
+            K.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                          mode=K.MODE_SEGMENT, segment_len=64, stream=s)
+    assert ei.value.status == 6
+    torch.cuda.synchronize()
+    # after a warm-up call on that stream the same call captures and replays
+    out = torch.empty_like(inp["q"])
+    with torch.cuda.stream(s):
+        K.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                      out=out, mode=K.MODE_SEGMENT, segment_len=64, stream=s)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        K.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                      out=out, mode=K.MODE_SEGMENT, segment_len=64, stream=s)
+    out.zero_()
+    g2.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
