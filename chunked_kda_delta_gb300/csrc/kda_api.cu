@@ -589,3 +589,145 @@ const char* kda_last_error_message(void) { return t_last_error; }
 const char* kda_version(void) { return "0.1.0"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Segment-parallel prefill that allocates nothing on the device.
+//
+// Some callers cannot call cudaMalloc at all: code running inside a CUDA graph that is
+// being captured (allocation is not a stream operation), allocators that own every
+// byte of device memory and forbid side allocations, and real-time services that must
+// not risk an allocation failure or the implicit device synchronisation of a first
+// allocation in the middle of a request.  kda_prefill_segment_noalloc() serves them:
+// its scratch (segment summaries, transitions and carries) lives in one fixed
+// file-scope device array, so no call allocates or frees anything.
+namespace {
+
+// 32 MiB: room for 512 fp32 128x128 state slots; a call needs B * H * (3 * nseg - 2).
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;
+
+struct NoAllocDevice {
+    bool ready = false;
+    void* scratch = nullptr;
+};
+NoAllocDevice g_noalloc[kMaxDevices];  // guarded by g_mutex
+
+}  // namespace
+
+// Held by every GPU that loads this library, until the process exits.  Host code must
+// not pass this name to a kernel: on the host it is only a stand-in for the symbol.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// Device address of the scratch array on `dev` (the current device), looked up once
+// per device with cudaGetSymbolAddress.
+kda_status noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    NoAllocDevice& d = g_noalloc[dev];
+    if (!d.ready) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+        d.scratch = ptr;
+        d.ready = true;
+    }
+    *out = d.scratch;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q,
+                                                  const uint16_t* k, const uint16_t* v,
+                                                  const float* g, const uint16_t* beta,
+                                                  float scale, const float* initial_state,
+                                                  uint16_t* out, float* final_state,
+                                                  int32_t segment_len, void* stream_) {
+    t_last_error[0] = '\0';
+    cudaStream_t stream = (cudaStream_t)stream_;
+    Problem pr{};
+    kda_status st = validate_shape(shape, false, &pr);
+    if (st != KDA_OK) return st;
+    if (segment_len <= 0 || segment_len % kda::kChunk != 0)
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "segment_len must be a positive multiple of 16 (got %d)", segment_len);
+    if ((st = validate_pointers(pr, q, k, v, g, beta, scale, initial_state, nullptr, out,
+                                final_state)) != KDA_OK)
+        return st;
+    const SegPlan sp = plan_segments(pr, segment_len);
+    if (sp.bytes > kNoAllocScratchBytes)
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "this shape needs %zu bytes of segment scratch; the no-allocation entry "
+                    "point has %zu (at most %zu state slots of 64 KiB, B*H*(3*nseg-2))",
+                    sp.bytes, kNoAllocScratchBytes, kNoAllocScratchBytes / (64 * 1024));
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo* di = nullptr;
+    if ((st = device_info(dev, &di)) != KDA_OK) return st;
+    void* scratch = nullptr;
+    if ((st = noalloc_scratch(dev, &scratch)) != KDA_OK) return st;
+    if (pr.T_total == 0 && !final_state) return KDA_OK;
+
+    kda::FwdParams p{};
+    p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16*>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16*>(v);
+    p.g = g;
+    p.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
+    p.s0 = initial_state;
+    p.sfin = final_state;
+    p.out = reinterpret_cast<__nv_bfloat16*>(out);
+    p.cu = nullptr;
+    p.T_total = pr.T_total;
+    p.dense_len = pr.dense_len;
+    p.N = pr.N;
+    p.H = pr.H;
+    p.scale = scale;
+    p.wait_limit = kDefaultWaitLimit;
+    p.status = di->status;
+    kda::TensorMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (pr.T_total > 0) {
+        if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "q")) ||
+            (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "k")) ||
+            (st = encode_chunk_map(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "v")) ||
+            (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")))
+            return st;
+    }
+    if (sp.nseg <= 1) {  // one segment: the plain serial pass, no scratch
+        if ((e = kda::launch_serial(p, maps, stream)) != cudaSuccess)
+            return cuda_fail(e, "prefill launch");
+        return KDA_OK;
+    }
+    // Every scratch byte a call reads is written earlier in the same call (summaries and
+    // transitions by pre_scan, carries by merge), so nothing needs clearing first.
+    float* b_seg = reinterpret_cast<float*>(static_cast<char*>(scratch) + sp.off_b);
+    float* m_seg = reinterpret_cast<float*>(static_cast<char*>(scratch) + sp.off_m);
+    float* carries = reinterpret_cast<float*>(static_cast<char*>(scratch) + sp.off_c);
+    kda::FwdParams ps = p;
+    ps.seg_len = segment_len;
+    ps.nseg_total = sp.nseg;
+    ps.nseg_used = sp.nseg - 1;
+    ps.s0 = nullptr;
+    ps.sfin = b_seg;
+    ps.flags = kda::kFlagNoOutput;
+    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
+        return cuda_fail(e, "pre_scan (summary) launch");
+    ps.sfin = m_seg;
+    ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0;
+    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
+        return cuda_fail(e, "pre_scan (transition) launch");
+    if ((e = kda::launch_merge(m_seg, b_seg, initial_state, carries, pr.N, sp.nseg, pr.H,
+                               stream)) != cudaSuccess)
+        return cuda_fail(e, "merge launch");
+    kda::FwdParams pk = p;
+    pk.seg_len = segment_len;
+    pk.nseg_total = sp.nseg;
+    pk.nseg_used = sp.nseg;
+    pk.s0 = carries;
+    pk.flags = kda::kFlagFinalLastSeg;
+    if ((e = kda::launch_serial(pk, maps, stream)) != cudaSuccess)
+        return cuda_fail(e, "segment-K2 launch");
+    return KDA_OK;
+}

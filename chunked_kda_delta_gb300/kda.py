@@ -29,7 +29,7 @@ _STATUS = {
 EXPORTED_SYMBOLS = (
     "kda_prefill", "kda_prefill_ex", "kda_prefill_host", "kda_workspace_bytes",
     "kda_get_device_status", "kda_release_workspaces", "kda_status_string",
-    "kda_last_error_message", "kda_version",
+    "kda_last_error_message", "kda_version", "kda_prefill_segment_noalloc",
 )
 
 
@@ -78,6 +78,9 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False) -> 
         lib.kda_prefill.argtypes = args
         lib.kda_prefill_ex.argtypes = args + [ctypes.POINTER(KdaOptions)]
         lib.kda_prefill_host.argtypes = args + [ctypes.POINTER(KdaOptions)]
+        lib.kda_prefill_segment_noalloc.argtypes = [
+            ctypes.POINTER(KdaShape), u16p, u16p, u16p, f32p, u16p, ctypes.c_float, f32p, u16p,
+            f32p, ctypes.c_int32, vp]
         lib.kda_workspace_bytes.argtypes = [ctypes.POINTER(KdaShape), ctypes.POINTER(KdaOptions),
                                             ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
@@ -87,6 +90,7 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False) -> 
         lib.kda_last_error_message.restype = ctypes.c_char_p
         lib.kda_version.restype = ctypes.c_char_p
         for f in (lib.kda_prefill, lib.kda_prefill_ex, lib.kda_prefill_host,
+                  lib.kda_prefill_segment_noalloc,
                   lib.kda_workspace_bytes, lib.kda_get_device_status,
                   lib.kda_release_workspaces):
             f.restype = ctypes.c_int
@@ -270,3 +274,35 @@ def kda_release_workspaces(device: int = -1) -> None:
     """Free the library's workspaces on ``device`` (-1: all devices)."""
     lib = load_library()
     _check(lib, lib.kda_release_workspaces(int(device)))
+
+
+def kda_prefill_segment_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                                g: torch.Tensor, beta: torch.Tensor, out: torch.Tensor,
+                                segment_len: int, scale: Optional[float] = None,
+                                initial_state: Optional[torch.Tensor] = None,
+                                final_state: Optional[torch.Tensor] = None, stream=None):
+    """Segment-parallel prefill with no device allocation (dense input only).
+
+    For callers that cannot allocate device memory: the library keeps the segment
+    scratch in a fixed 32 MiB device array shared by all calls, so ``out`` (and
+    ``final_state`` when wanted) must be passed in.  Shapes needing more than
+    B * H * (3 * nseg - 2) = 512 state slots are rejected; calls overlapping on the
+    GPU race on the shared array.  The first call on a device must precede any
+    stream capture.
+    """
+    lib = load_library()
+    _check_tensors(q, k, v, g, beta, initial_state, None, "cuda")
+    shape = _shape_of(q, None)
+    if scale is None:
+        scale = shape.head_dim ** -0.5
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    with torch.cuda.device(q.device):
+        st = lib.kda_prefill_segment_noalloc(
+            ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+            ctypes.c_float(scale), _ptr(initial_state), _ptr(out), _ptr(final_state),
+            int(segment_len), ctypes.c_void_p(int(stream)))
+    _check(lib, st)
+    return out, final_state

@@ -138,6 +138,30 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
                             const int32_t* cu_seqlens, uint16_t* out, float* final_state,
                             void* stream, const kda_options* opts);
 
+/* kda_prefill_segment_noalloc -- segment-parallel prefill that allocates no device
+ * memory.  The pages have no counterpart: this entry point exists for callers that
+ * cannot call cudaMalloc (code inside a stream capture, applications whose allocator
+ * owns all device memory, services that must not allocate in a request), as a variant
+ * of segment mode (kda_prefill_ex with KDA_MODE_SEGMENT) whose scratch lives in one
+ * fixed 32 MiB device array inside the library.
+ *   Arguments as kda_prefill for dense input (no cu_seqlens); segment_len is the
+ *   segment length in tokens, a positive multiple of 16.
+ *   Limit: B * H * (3 * nseg - 2) <= 512, nseg = ceil(seq_len / segment_len) (each
+ *   term a 64 KiB fp32 state); larger shapes return KDA_ERR_INVALID_ARGUMENT before any
+ *   device work.  A single segment needs no scratch.
+ *   The array is shared by every call in the process and keeps the last call's
+ *   contents; no part of it needs to start at zero (each call writes every byte it
+ *   reads).  Calls that overlap on the GPU (other streams, other threads) race on it:
+ *   serialise them.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any
+ *   stream capture.  Every GPU that loads the library holds the 32 MiB until exit. */
+kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q,
+                                       const uint16_t* k, const uint16_t* v, const float* g,
+                                       const uint16_t* beta, float scale,
+                                       const float* initial_state, uint16_t* out,
+                                       float* final_state, int32_t segment_len, void* stream);
+
 /* Bytes of device workspace a call with this shape and these options uses
  * (0 for serial mode).  No device work; *bytes is written on success. */
 kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, size_t* bytes);
