@@ -373,7 +373,8 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
         if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "q")) ||
             (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "k")) ||
             (st = encode_chunk_map(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "v")) ||
-            (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")))
+            (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")) ||
+            (st = encode_chunk_map(&maps.out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "out")))
             return st;
     }
     const SegPlan sp = mode == KDA_MODE_SEGMENT ? plan_segments(pr, seg_len) : SegPlan{};
@@ -692,7 +693,8 @@ extern "C" kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const 
         if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "q")) ||
             (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "k")) ||
             (st = encode_chunk_map(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "v")) ||
-            (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")))
+            (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")) ||
+            (st = encode_chunk_map(&maps.out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "out")))
             return st;
     }
     if (sp.nseg <= 1) {  // one segment: the plain serial pass, no scratch

@@ -1,5 +1,6 @@
-// kda_fwd_tc.cu -- fused K1 + K2 KDA forward prefill for sm_103a: TMA-staged chunk
-// tiles, tcgen05 MMAs with the state held in tensor memory (TMEM) across all chunks.
+// kda_fwd_tc.cu -- fused K1 + K2 KDA forward prefill for sm_103a: one 2-CTA thread-block
+// cluster per (sequence, head); TMA-staged chunk tiles; tcgen05 MMAs with the state held
+// in tensor memory (TMEM) across all chunks.
 //
 // The method (cuLA PR #103 "feat(kda/sm90): FlashKDA prefill port + intracard-CP
 // prefill", commit notes: "K1 prepares decayed q/k, beta and the WY inverse; K2 runs
@@ -25,18 +26,28 @@
 //   delta^T = U^T - sum(P_W)   (K2 threads, written back to TMEM as bf16)
 //   MMA2: S^T += delta^T . Kbar   (after the K2 threads scaled S^T by exp(gam_C))
 //   MMA3: P_Q += delta^T . Mq^T;  O^T = scale * sum(P_Q)
-// Warp roles (448 threads): warp 0 TMA producer (and beta, prefetched two chunks
-// ahead); warp 1 TMEM owner; warps 2-5 K1 (cumulative decay, decayed operands,
-// in-chunk Grams and the WY solve; the 16x16 products use mma.sync because tcgen05's
-// smallest M is 64); warps 6-13 K2: state conversion/decay, delta, output, and the
-// tcgen05 MMAs themselves.  The tensor pipe runs the MMAs of one issuing thread one
-// after another but overlaps those of different warps, so each K2 warp issues its own
-// slice: MMA1 is split over the 4 K-quarters into partial accumulators (the warps of
-// one half for S W^T, of the other for S Qtil^T), and the state update into two N=64
-// halves plus Mq delta, issued by three warps.  K2 warps meet at a named barrier
-// instead of handing work to a separate issuing warp.
-// Every wait is bounded: on exhaustion the kernel records KDA_ERR_DEVICE_TIMEOUT
-// in the status word, drains its in-flight copies and MMAs and exits.
+//
+// Work split (416 threads per CTA, 13 warps):
+//   CTA rank 0 ("K1 CTA"): warp 0 is the TMA producer (q/k/v/g tiles into a 4-stage
+//     ring; beta with plain loads, prefetched two chunks ahead); warps 1-12 are three
+//     K1 groups of 4 warps taking every third chunk (cumulative decay, decayed operands,
+//     in-chunk Grams and the WY solve; the 16x16 products use mma.sync because
+//     tcgen05's smallest M is 64).  A group writes its chunk's operands (21.8 KB) into
+//     a local buffer and ships them to the K2 CTA with one cp.async.bulk
+//     shared::cta -> shared::cluster copy that completes the K2 CTA's barrier.
+//   CTA rank 1 ("K2 CTA"): warp 0 owns TMEM; warps 1-8 run the state chain: state
+//     conversion/decay, delta, output, and the tcgen05 MMAs themselves.  The tensor
+//     pipe runs the MMAs of one issuing thread one after another but overlaps those of
+//     different warps, so MMA1 is split over the 4 K-quarters into partial accumulators
+//     issued by 4 warps (N = 32: W and Qtil together), and the state update (N = 128)
+//     and Mq delta are issued by two more.  Output rows of full chunks are staged in
+//     shared memory and written by one TMA tensor store per chunk.  K2 hands its
+//     3-stage receive ring back to K1 with remote mbarrier arrivals.
+// Splitting a chain over two SMs doubles the shared-memory bandwidth and issue slots
+// each chunk gets; one SM alone was bound by its shared-memory pipe.
+// Every wait is bounded: on exhaustion the kernel records KDA_ERR_DEVICE_TIMEOUT in the
+// status word, drains its in-flight copies and MMAs, meets its peer at the final
+// cluster barrier and exits.
 #include <cuda.h>
 
 #include "kda_internal.cuh"
@@ -47,7 +58,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 448;
+constexpr int kK1Groups = 3;                    // K1 groups, chunk c -> group c % 3
+constexpr int kThreads = 32 * (1 + 4 * kK1Groups);  // 416
 constexpr int kRef = 7;
 constexpr uint32_t kTmemCols = 512;
 // Bound of the waits that drain in-flight copies and MMAs before exit; independent of
@@ -55,41 +67,55 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int64_t kDrainLimit = 1ll << 24;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// TMEM column map
+// TMEM column map (K2 CTA)
 constexpr uint32_t kColS = 0;     // S^T fp32, 128 columns
 constexpr uint32_t kColSA = 128;  // S^T bf16 pairs, 64 columns (MMA1 A operand)
-constexpr uint32_t kColDd = 192;  // 4 partials x 16 columns of S^T W^T
-constexpr uint32_t kColDO = 256;  // 2 buffers x 4 partials x 16 columns of S^T Qtil^T (+ delta^T Mq^T)
-constexpr uint32_t kColDA = 384;  // delta^T bf16 pairs, 8 columns (MMA2/MMA3 A operand)
+// MMA1 accumulators: 2 buffers x 4 K-quarter partials x 32 columns; in each partial,
+// columns 0-15 hold S^T W^T and 16-31 hold S^T Qtil^T (+ delta^T Mq^T in partial 0).
+constexpr uint32_t kColD1 = 192;
+constexpr uint32_t kColDA = 448;  // delta^T bf16 pairs, 8 columns (MMA2/MMA3 A operand)
 
-// Shared memory map (bytes)
+// Input stage (K1 CTA): q, k, v bf16 [16][128]; g fp32 [16][128]; beta fp32 [16].
 constexpr int kInQ = 0, kInK = 4096, kInV = 8192, kInG = 12288, kInBeta = 20480;
 constexpr int kInBytes = 20608;
+constexpr int kInStages = 4;
 constexpr uint32_t kTxBytes = 20480;  // q, k, v, g tiles
-// U rows are padded to 132 floats so that the fragment-layout float2 stores of the
-// 16x8 MMA tiles (8 rows x 4 lanes) hit 32 distinct banks.
+// Chunk operand stage (K1 -> K2): B1 = [W ; Qtil] (N=32, K=128), B2 = Kbar (N=128,
+// K=16), B3 = Mq (N=16, K=16), all bf16 in the no-swizzle K-major layout; U fp32 rows
+// padded to 132 floats so the fragment-layout float2 stores hit 32 distinct banks;
+// exp(gam_C) fp32 [128].
 constexpr int kURow = 132;
 constexpr int kB1 = 0, kB2 = 8192, kB3 = 12288, kU = 12800, kGC = kU + 16 * kURow * 4,
               kOutBytes = kGC + 512;
+constexpr int kRecvStages = 3;
 constexpr uint32_t kLbo = 128, kSboB1 = 2048, kSboB2 = 256, kSboB3 = 256;
-constexpr int kStRow = 272, kStArr = 16 * kStRow;  // padded bf16 staging rows (136 elems)
+// K1 group scratch: padded bf16 staging rows (136 elements), exp(gam_ref), A, Tb, beta.
+constexpr int kStRow = 272, kStArr = 16 * kStRow;
 enum { ST_KQ = 0, ST_QQ, ST_KK, ST_VV, ST_NUM };
-constexpr int kSmIn = 0;                               // 2 input stages
-constexpr int kSmOut = kSmIn + 2 * kInBytes;           // 2 K1 output stages
-constexpr int kSmSt = kSmOut + 2 * kOutBytes;          // staging
-constexpr int kSmEref = kSmSt + ST_NUM * kStArr;       // fp32 128: exp(gam_ref)
-constexpr int kSmA = kSmEref + 512;                    // fp32 16x16
-constexpr int kSmTb = kSmA + 1024;                     // bf16 16x24
-constexpr int kSmBeta = kSmTb + 768;                   // fp32 16 (K1 copy)
-constexpr int kSmBar = kSmBeta + 64;                   // mbarriers
+constexpr int kGEref = ST_NUM * kStArr, kGA = kGEref + 512, kGTb = kGA + 1024,
+              kGBeta = kGTb + 768, kGrpBytes = kGBeta + 64;
+// Shared memory map.  K1 CTA: input ring, 2 group scratches, 2 local operand stages.
+// K2 CTA: receive ring at offset 0.  Barriers sit at the same offset in both.
+constexpr int kSmIn = 0;
+constexpr int kSmGrp = kSmIn + kInStages * kInBytes;
+constexpr int kSmOutLocal = kSmGrp + kK1Groups * kGrpBytes;
+constexpr int kSmRecv = 0;
+constexpr int kSmOTile = kSmRecv + kRecvStages * kOutBytes;  // K2 CTA: 2 output tiles bf16 [16][128]
+constexpr int kOTileBytes = kChunk * kD * 2;
+constexpr int kSmBar = kSmOutLocal + kK1Groups * kOutBytes;
 constexpr int kNumBars = 16;
 constexpr int kSmTmemSlot = kSmBar + kNumBars * 8;
-constexpr int kSmemBytes = kSmTmemSlot + 16;
-enum {
-    BAR_IN_FULL = 0, BAR_IN_EMPTY = 2, BAR_K1_FULL = 4, BAR_K1_EMPTY = 6,
-    BAR_D1 = 8, BAR_SDONE = 9, BAR_DRAIN = 10, BAR_NEVER = 11
+constexpr int kSmFail = kSmTmemSlot + 8;            // int32 per K1 group: failure flags
+constexpr int kSmemBytes = kSmFail + 4 * kK1Groups;
+static_assert(kSmOTile + 2 * kOTileBytes <= kSmBar, "K2 buffers overlap the barriers");
+static_assert(kSmOTile % 128 == 0, "TMA store source must be 128-byte aligned");
+enum {  // K1 CTA barriers
+    BAR_IN_FULL = 0, BAR_IN_EMPTY = 4, BAR_OUT_FREE = 8
 };
-constexpr uint32_t kNamedK1 = 1, kNamedK2 = 2;
+enum {  // K2 CTA barriers
+    BAR_K1_FULL = 0, BAR_D1 = 3, BAR_SDONE = 4, BAR_DRAIN = 5, BAR_NEVER = 6
+};
+constexpr uint32_t kNamedK2 = 1 + kK1Groups;  // K1 groups use named barriers 1 .. kK1Groups
 
 __device__ __forceinline__ uint32_t b1_off(int n, int k) {
     return (n >> 3) * kSboB1 + (k >> 3) * kLbo + (n & 7) * 16 + (k & 7) * 2;
@@ -131,14 +157,16 @@ __device__ __forceinline__ void gram16(uint32_t abase, uint32_t bbase, int lane,
 __global__ void __launch_bounds__(kThreads, 1)
 kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                  const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_out, const FwdParams p) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % p.H;
-    const int n = blockIdx.x / p.H;
+    const uint32_t rank = cluster_ctarank();   // 0: K1 CTA, 1: K2 CTA
+    const int unit = blockIdx.x >> 1;          // (row, head) of this cluster
+    const int h = unit % p.H;
+    const int n = unit / p.H;
     int64_t bos, eos;
-    if (!seq_range(p, n, bos, eos)) return;
+    if (!seq_range(p, n, bos, eos)) return;   // both CTAs of the cluster return
     const int64_t H = p.H;
     const int nchunks = (int)((eos - bos + kChunk - 1) / kChunk);
     const int64_t lim = p.wait_limit;
@@ -146,36 +174,42 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t bars = sbase + kSmBar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmTmemSlot);
+    volatile int32_t* fail_flag = reinterpret_cast<volatile int32_t*>(smem + kSmFail);
 
     if (tid == 0) {
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(BAR_IN_FULL + s), 1);
-            mbar_init(bar(BAR_IN_EMPTY + s), 1);
-            mbar_init(bar(BAR_K1_FULL + s), 4);   // one arrival per K1 warp
-            mbar_init(bar(BAR_K1_EMPTY + s), 8);  // one arrival per epilogue warp
+        if (rank == 0) {
+            for (int s = 0; s < kInStages; ++s) {
+                mbar_init(bar(BAR_IN_FULL + s), 1);
+                mbar_init(bar(BAR_IN_EMPTY + s), 1);
+            }
+            for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_OUT_FREE + s), 8);
+            for (int gi = 0; gi < kK1Groups; ++gi) fail_flag[gi] = 0;
+        } else {
+            for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_K1_FULL + s), 1);
+            mbar_init(bar(BAR_D1), 4);     // one commit per MMA1 slice (K-quarter)
+            mbar_init(bar(BAR_SDONE), 2);  // the state update and Mq delta
+            mbar_init(bar(BAR_DRAIN), 8);
+            mbar_init(bar(BAR_NEVER), 1);  // never signalled (timeout-path test)
         }
-        mbar_init(bar(BAR_D1), 8);     // one commit per K2 warp (MMA1 slices)
-        mbar_init(bar(BAR_SDONE), 3);  // commits of the two state-update halves and Mq delta
-        mbar_init(bar(BAR_DRAIN), 8);
-        mbar_init(bar(BAR_NEVER), 1);  // never signalled (timeout-path test)
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (rank == 1 && warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0 && nchunks > 0) {
+    if (rank == 0 && warp == 0 && lane == 0 && nchunks > 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_g);
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // barriers of both CTAs initialised before any remote access
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem = tmem_base;
 
-    if (warp == 0) {
+    if (rank == 0 && warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // beta is read with plain loads two chunks ahead (its [T][H] rows are 2 bytes
         // wide, below the 16-byte TMA granule) and stored next to the TMA tiles.
@@ -187,8 +221,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float b_cur = load_beta(0), b_next = load_beta(1);
         int issued = 0;
         for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1;
-            const bool ok = c < 2 || mbar_wait(bar(BAR_IN_EMPTY + s), ((c >> 1) - 1) & 1, lim);
+            const int s = c % kInStages;
+            const bool ok = c < kInStages ||
+                            mbar_wait(bar(BAR_IN_EMPTY + s), ((c / kInStages) - 1) & 1, lim);
             if (__any_sync(0xffffffffu, !ok)) {
                 if (lane == 0) record(p.status, kStatusTimeout);
                 break;
@@ -211,37 +246,40 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         // Drain: every issued load must have landed before the CTA exits.
         if (lane == 0)
-            for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c)
-                if (!mbar_wait(bar(BAR_IN_FULL + (c & 1)), (c >> 1) & 1, kDrainLimit))
+            for (int c = (issued >= kInStages ? issued - kInStages : 0); c < issued; ++c)
+                if (!mbar_wait(bar(BAR_IN_FULL + (c % kInStages)), (c / kInStages) & 1, kDrainLimit))
                     record(p.status, kStatusTimeout);
-    } else if (warp == 1) {
-        // TMEM owner: allocated above, released after the final barrier.
-    } else if (warp < 6) {
-        // ------------------------------------------------------------ K1 (128 threads)
-        const int kt = tid - 64;          // 0..127
-        const int kw = kt >> 5;           // K1 warp 0..3
+    } else if (rank == 0) {
+        // ------------------------------------------------------------ K1 groups (kK1Groups x 128 threads)
+        const int gi = (warp - 1) >> 2;   // group: chunks c with c % kK1Groups == gi
+        const uint32_t nbar = 1 + gi;     // named barrier of the group
+        const int kt = tid - 32 - 128 * gi;
+        const int kw = kt >> 5;           // warp within the group
         const int pc = kt & 63;           // channel pair: channels 2pc, 2pc+1
         const int hr = kt >> 6;           // row half: rows 8hr .. 8hr+7
-        unsigned char* st = smem + kSmSt;
-        float* eref_sm = reinterpret_cast<float*>(smem + kSmEref);
-        float* Asm = reinterpret_cast<float*>(smem + kSmA);
-        __nv_bfloat16* Tb = reinterpret_cast<__nv_bfloat16*>(smem + kSmTb);
-        float* bet = reinterpret_cast<float*>(smem + kSmBeta);
+        unsigned char* grp = smem + kSmGrp + gi * kGrpBytes;
+        unsigned char* st = grp;
+        float* eref_sm = reinterpret_cast<float*>(grp + kGEref);
+        float* Asm = reinterpret_cast<float*>(grp + kGA);
+        __nv_bfloat16* Tb = reinterpret_cast<__nv_bfloat16*>(grp + kGTb);
+        float* bet = reinterpret_cast<float*>(grp + kGBeta);
+        unsigned char* ob = smem + kSmOutLocal + gi * kOutBytes;
         const float2 l2e2 = make_float2(kLog2e, kLog2e), nl2e2 = make_float2(-kLog2e, -kLog2e);
         const bool zero_v = (p.flags & kFlagZeroV) != 0;
         const bool with_out = (p.flags & kFlagNoOutput) == 0;
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1, ks = c & 1;
-            bool ok = mbar_wait(bar(BAR_IN_FULL + s), (c >> 1) & 1, lim);
-            if (ok && c >= 2) ok = mbar_wait(bar(BAR_K1_EMPTY + ks), ((c >> 1) - 1) & 1, lim);
-            if (named_bar_or(kNamedK1, 128, !ok)) {
+        for (int c = gi; c < nchunks; c += kK1Groups) {
+            const int s = c % kInStages;
+            bool ok = mbar_wait(bar(BAR_IN_FULL + s), (c / kInStages) & 1, lim) && !fail_flag[gi];
+            // The local operand buffer is rewritten below: the previous copy out of it
+            // must have finished reading.
+            if (kt == 0 && c >= kK1Groups) bulk_wait_read0();
+            if (named_bar_or(nbar, 128, !ok)) {
                 if (kt == 0) record(p.status, kStatusTimeout);
                 break;
             }
             const int64_t t0 = bos + (int64_t)c * kChunk;
             const int C = (eos - t0 < kChunk) ? (int)(eos - t0) : kChunk;
             const unsigned char* in = smem + kSmIn + s * kInBytes;
-            unsigned char* ob = smem + kSmOut + ks * kOutBytes;
             if (kt < kChunk) bet[kt] = reinterpret_cast<const float*>(in + kInBeta)[kt];
 
             // Phase 1: cumulative decay (log2 units) and decayed operands for
@@ -306,7 +344,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 *reinterpret_cast<uint4*>(b2 + (c1 >> 3) * kSboB2 + hr * kLbo + (c1 & 7) * 16) =
                     make_uint4(kb1[0], kb1[1], kb1[2], kb1[3]);
             }
-            named_bar_sync(kNamedK1, 128);
+            named_bar_sync(nbar, 128);
             if (kt == 0) mbar_arrive(bar(BAR_IN_EMPTY + s));  // input tiles consumed
 
             // Phase 2: warp 0 Gram A and the WY solve; warp 1 Gram Mq; warps 2-3 write
@@ -379,7 +417,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                    pack_bf16(x2.x, x2.y), pack_bf16(x3.x, x3.y));
                 }
             }
-            named_bar_sync(kNamedK1, 128);
+            named_bar_sync(nbar, 128);
 
             // Phase 3: W = (Tb (K o exp(gam - gam_ref))) o exp(gam_ref), U = Tb V;
             // K1 warp kw owns columns [32kw, 32kw + 32).
@@ -421,20 +459,40 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
             fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_K1_FULL + ks));
+            named_bar_sync(nbar, 128);
+            if (kt == 0) {
+                // Ship the chunk's operands into the K2 CTA's receive stage.
+                const int os = c % kRecvStages;
+                bool free_ok = c < kRecvStages ||
+                               mbar_wait_cluster(bar(BAR_OUT_FREE + os), ((c / kRecvStages) - 1) & 1, lim);
+                if (free_ok) {
+                    const uint32_t rbar = mapa(bar(BAR_K1_FULL + os), 1);
+                    mbar_arrive_expect_tx_remote(rbar, (uint32_t)kOutBytes);
+                    bulk_copy_to_peer(mapa(sbase + kSmRecv + os * kOutBytes, 1), smem_u32(ob),
+                                      (uint32_t)kOutBytes, rbar);
+                    bulk_commit();
+                } else {
+                    fail_flag[gi] = 1;
+                }
+            }
         }
+        if (kt == 0) bulk_wait0();  // every copy into the peer completed before exit
+    } else if (warp == 0 || warp > 8) {
+        // TMEM owner (warp 0): allocated above, released after the final barrier.
+        // Warps 9+ of the K2 CTA exist because both CTAs share one block size.
     } else {
-        // ------------------------------------------------------------ K2 (256 threads)
+        // ------------------------------------------------------------ K2 state chain (256 threads)
         const int quad = warp & 3;                 // TMEM lane quadrant = SM sub-partition
-        const int hf = (warp - 6) >> 2;            // 0: key columns 0-63, 1: 64-127
+        const int hf = (warp - 1) >> 2;            // 0: key columns 0-63, 1: 64-127
         const int j = 32 * quad + lane;            // value column owned by this thread
         const uint32_t lanes = (uint32_t)(32 * quad) << 16;
         const uint32_t tS = tmem + lanes + kColS + 64u * hf;
         const uint32_t tSA = tmem + lanes + kColSA + 32u * hf;
         const uint32_t tDA = tmem + lanes + kColDA + 4u * hf;
-        const uint32_t idesc16 = idesc_bf16(128, 16), idesc64 = idesc_bf16(128, 64);
+        const uint32_t idesc32 = idesc_bf16(128, 32), idesc128 = idesc_bf16(128, 128),
+                       idesc16 = idesc_bf16(128, 16);
         const bool with_out = (p.flags & kFlagNoOutput) == 0;
+        const bool store_issuer = warp == 1;       // issues (and drains) the TMA stores
         // State rows: initial state at this CTA's row; final state at its row, or (segment
         // runs) at sequence b for the last segment only.
         const size_t soff = ((size_t)n * p.H + h) * kD * kD;
@@ -458,13 +516,15 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_st32(tS, sreg);
         tmem_st32(tS + 32, sreg + 32);
         tmem_wait_st();
-        // Sum over the 4 K-quarter partials of 8 accumulator columns (rows 8hf..8hf+7).
-        auto ld_partials = [&](uint32_t col0, float (&v)[8]) {
+        // Sum over the 4 K-quarter partials of 8 accumulator columns (rows 8hf..8hf+7);
+        // `col` selects the S^T W^T (0) or the output (16) half of each partial.
+        auto ld_partials = [&](uint32_t buf, uint32_t col, float (&v)[8]) {
             uint32_t a[8], b[8], c2[8], d[8];
-            tmem_ld8(tmem + lanes + col0 + 8 * hf, a);
-            tmem_ld8(tmem + lanes + col0 + 16 + 8 * hf, b);
-            tmem_ld8(tmem + lanes + col0 + 32 + 8 * hf, c2);
-            tmem_ld8(tmem + lanes + col0 + 48 + 8 * hf, d);
+            const uint32_t base = tmem + lanes + kColD1 + 128u * buf + col + 8 * hf;
+            tmem_ld8(base, a);
+            tmem_ld8(base + 32, b);
+            tmem_ld8(base + 64, c2);
+            tmem_ld8(base + 96, d);
             tmem_wait_ld_regs<8>(a);
             tmem_wait_ld_regs<8>(b);
             tmem_wait_ld_regs<8>(c2);
@@ -474,31 +534,59 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 v[r] = (__uint_as_float(a[r]) + __uint_as_float(b[r])) +
                        (__uint_as_float(c2[r]) + __uint_as_float(d[r]));
         };
-        auto store_out = [&](int cp) {
+        // Output rows of chunk cp: a full chunk goes through a shared-memory tile and one
+        // TMA store (issued after the next K2 barrier); the ragged last chunk of a
+        // sequence is written with plain stores so that no row past the sequence is
+        // touched.  Returns true when a tile was filled.
+        auto emit_out = [&](int cp) -> bool {
             const int64_t t0p = bos + (int64_t)cp * kChunk;
             const int Cp = (eos - t0p < kChunk) ? (int)(eos - t0p) : kChunk;
             float o[8];
-            ld_partials(kColDO + 64u * (cp & 1), o);
+            ld_partials(cp & 1, 16, o);
+            if (Cp == kChunk) {
+                __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem + kSmOTile + (cp & 1) * kOTileBytes);
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    tile[(8 * hf + r) * kD + j] = __float2bfloat16_rn(p.scale * o[r]);
+                fence_proxy_async_smem();
+                return true;
+            }
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int row = 8 * hf + r;
                 if (row < Cp)
                     p.out[((t0p + row) * H + h) * kD + j] = __float2bfloat16_rn(p.scale * o[r]);
             }
+            return false;
+        };
+        int tile_pending = -1;  // chunk whose tile awaits its TMA store
+        auto issue_tile_store = [&]() {
+            if (tile_pending >= 0 && store_issuer && elect_one()) {
+                const int32_t t0p = (int32_t)(bos + (int64_t)tile_pending * kChunk);
+                tma_store_3d(&tm_out, sbase + kSmOTile + (tile_pending & 1) * kOTileBytes, 0, h, t0p);
+                bulk_commit();
+            }
+            __syncwarp();
+            tile_pending = -1;
         };
         bool ok = true;
         if (p.debug_flags & 1) ok = mbar_wait(bar(BAR_NEVER), 0, lim);  // nothing signals it
         if (named_bar_or(kNamedK2, 256, !ok)) ok = false;
         for (int c = 0; ok && c < nchunks; ++c) {
-            const int ks = c & 1;
-            const uint32_t ob = sbase + kSmOut + ks * kOutBytes;
-            bool w = mbar_wait(bar(BAR_K1_FULL + ks), (c >> 1) & 1, lim);
+            const int ks = c % kRecvStages;
+            const uint32_t ob = sbase + kSmRecv + ks * kOutBytes;
+            bool w = mbar_wait_cluster(bar(BAR_K1_FULL + ks), (c / kRecvStages) & 1, lim);
             if (c > 0) w = w && mbar_wait(bar(BAR_SDONE), (c - 1) & 1, lim);
+            // The tile being refilled this iteration (chunk c-1's buffer, last stored from
+            // chunk c-3) must have been read by its TMA store.
+            if (store_issuer && lane == 0) bulk_wait_read0();
             if (named_bar_or(kNamedK2, 256, !w)) { ok = false; break; }
             tc_fence_after();
-            // The previous chunk's K1 stage is no longer read (its U and exp(gam_C) were
-            // consumed last iteration; the MMAs reading B1..B3 completed).
-            if (c > 0 && lane == 0) mbar_arrive(bar(BAR_K1_EMPTY + ((c - 1) & 1)));
+            issue_tile_store();
+            // The previous chunk's stage is no longer read (its U and exp(gam_C) were
+            // consumed last iteration; the MMAs reading B1..B3 completed): hand it back.
+            if (c > 0 && lane == 0)
+                mbar_arrive_remote_relaxed(mapa(bar(BAR_OUT_FREE + (c - 1) % kRecvStages), 0));
             // (A) S_c (this half) -> bf16 copy for MMA1
             tmem_ld32(tS, sreg);
             tmem_ld32(tS + 32, sreg + 32);
@@ -514,28 +602,25 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_before();
             named_bar_sync(kNamedK2, 256);
             tc_fence_after();
-            // MMA1 slice of this warp: K-quarter `quad`; half 0 -> S^T W^T partial,
-            // half 1 -> S^T Qtil^T partial (not needed without output rows).
-            if (elect_one()) {
-              if (hf == 0 || with_out) {
-                const uint32_t bb = ob + kB1 + (uint32_t)hf * 2u * kSboB1;
-                const uint32_t d = hf == 0 ? tmem + kColDd + 16u * quad
-                                           : tmem + kColDO + 64u * (c & 1) + 16u * quad;
+            // MMA1 slice: warps of half 0 take K-quarter `quad`; N = 32 covers W and Qtil
+            // (only W without output rows).
+            if (hf == 0) {
+                if (elect_one()) {
+                    const uint32_t d = tmem + kColD1 + 128u * (c & 1) + 32u * quad;
 #pragma unroll
-                for (int s2 = 0; s2 < 2; ++s2) {
-                    const int kk = 2 * quad + s2;
-                    mma_ts(d, tmem + kColSA + 8u * kk, sdesc(bb + kk * 2 * kLbo, kLbo, kSboB1),
-                           idesc16, s2);
+                    for (int s2 = 0; s2 < 2; ++s2) {
+                        const int kk = 2 * quad + s2;
+                        mma_ts(d, tmem + kColSA + 8u * kk,
+                               sdesc(ob + kB1 + kk * 2 * kLbo, kLbo, kSboB1),
+                               with_out ? idesc32 : idesc16, s2);
+                    }
+                    tc_commit(bar(BAR_D1));
                 }
-              }
-                tc_commit(bar(BAR_D1));
+                __syncwarp();
             }
-            __syncwarp();
-            // (C) output rows of the previous chunk
-            if (c > 0 && with_out) store_out(c - 1);
             // (D) decay S by exp(gam_C) ahead of the state update
             {
-                const float4* gc4 = reinterpret_cast<const float4*>(smem + kSmOut + ks * kOutBytes + kGC) + 16 * hf;
+                const float4* gc4 = reinterpret_cast<const float4*>(smem + kSmRecv + ks * kOutBytes + kGC) + 16 * hf;
 #pragma unroll
                 for (int i4 = 0; i4 < 16; ++i4) {
                     const float4 gv = gc4[i4];
@@ -556,8 +641,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (w) {
                 tc_fence_after();
                 float dsum[8];
-                ld_partials(kColDd, dsum);
-                const float* U = reinterpret_cast<const float*>(smem + kSmOut + ks * kOutBytes + kU);
+                ld_partials(c & 1, 0, dsum);
+                const float* U = reinterpret_cast<const float*>(smem + kSmRecv + ks * kOutBytes + kU);
                 uint32_t pk[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -570,28 +655,33 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_before();
             if (named_bar_or(kNamedK2, 256, !w)) { ok = false; break; }
             tc_fence_after();
-            // State update (two N=64 halves) and Mq delta into the first O partial.
-            if (hf == 0 && quad < 3) {
+            // State update (N = 128) and Mq delta into the output half of partial 0.
+            if (hf == 0 && quad < 2) {
                 if (elect_one()) {
-                    if (quad < 2)
-                        mma_ts(tmem + kColS + 64u * quad, tmem + kColDA,
-                               sdesc(ob + kB2 + quad * 8 * kSboB2, kLbo, kSboB2), idesc64, 1);
+                    if (quad == 0)
+                        mma_ts(tmem + kColS, tmem + kColDA, sdesc(ob + kB2, kLbo, kSboB2), idesc128, 1);
                     else if (with_out)
-                        mma_ts(tmem + kColDO + 64u * (c & 1), tmem + kColDA,
+                        mma_ts(tmem + kColD1 + 128u * (c & 1) + 16, tmem + kColDA,
                                sdesc(ob + kB3, kLbo, kSboB3), idesc16, 1);
                     tc_commit(bar(BAR_SDONE));
                 }
                 __syncwarp();
             }
+            // (C) output rows of the previous chunk, while the state update runs
+            if (c > 0 && with_out && emit_out(c - 1)) tile_pending = c - 1;
         }
         if (ok && nchunks > 0) {
             // Output of the last chunk and the final state.
             const bool w = mbar_wait(bar(BAR_SDONE), (nchunks - 1) & 1, lim);
+            if (store_issuer && lane == 0) bulk_wait_read0();
             if (named_bar_or(kNamedK2, 256, !w)) {
                 ok = false;
             } else {
                 tc_fence_after();
-                if (with_out) store_out(nchunks - 1);
+                issue_tile_store();
+                if (with_out && emit_out(nchunks - 1)) tile_pending = nchunks - 1;
+                named_bar_sync(kNamedK2, 256);
+                issue_tile_store();
             }
         }
         if (!ok) {
@@ -606,6 +696,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int i = 0; i < 64; ++i)
                 p.sfin[foff + (size_t)(64 * hf + i) * kD + j] = __uint_as_float(sreg[i]);
         }
+        if (store_issuer && lane == 0) bulk_wait0();  // TMA stores complete before exit
         // Drain every MMA this warp issued before TMEM is released.
         if (elect_one()) tc_commit(bar(BAR_DRAIN));
         __syncwarp();
@@ -613,10 +704,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 
     tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
+    cluster_sync();  // neither CTA leaves while its peer may still access its memory
+    if (rank == 1 && warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -627,11 +718,21 @@ const void* serial_kernel_symbol() { return reinterpret_cast<const void*>(&kda_f
 
 cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream_t stream) {
     const long long rows = p.seg_len > 0 ? (long long)p.N * p.nseg_used : (long long)p.N;
-    const long long blocks = rows * p.H;
-    if (blocks == 0) return cudaSuccess;
-    kda_fwd_tc_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, stream>>>(maps.q, maps.k, maps.v,
-                                                                          maps.g, p);
-    return cudaGetLastError();
+    const long long clusters = rows * p.H;
+    if (clusters == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kda_fwd_tc_kernel, maps.q, maps.k, maps.v, maps.g, maps.out, p);
 }
 
 }  // namespace kda

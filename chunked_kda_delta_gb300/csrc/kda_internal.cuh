@@ -80,6 +80,7 @@ __device__ __forceinline__ bool seq_range(const FwdParams& p, int n, int64_t& bo
 // one head).  Encoded on the host, passed to kernels as __grid_constant__ params.
 struct TensorMaps {
     CUtensorMap q, k, v, g;
+    CUtensorMap out;  // output (TMA stores of full chunks)
 };
 
 // Launchers (return the launch error, cudaSuccess on success).
