@@ -39,9 +39,17 @@ UNIT = "head-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 BYTES_PER_HEAD_TOKEN = 3 * 256 + 512 + 2 + 256   # q, k, v bf16 + g fp32 + beta + out
 STATE_BYTES = 128 * 128 * 4
-COMPUTE_DTYPE = "f32"      # arithmetic of the current serial kernel
-KERNEL_SOURCES = {"serial": ["chunked_kda_delta_gb300/csrc/kda_fwd_serial.cu"]}
-KERNEL_NAMES = {"serial": "kda_fwd_simple_kernel"}
+# Tensor-core operands are bf16 (fp32 accumulation); the state, decays and the WY
+# solve are fp32.
+COMPUTE_DTYPE = "bf16"
+_FWD_SOURCES = ["chunked_kda_delta_gb300/csrc/kda_fwd_tc.cu",
+                "chunked_kda_delta_gb300/csrc/kda_ptx.cuh",
+                "chunked_kda_delta_gb300/csrc/kda_internal.cuh"]
+KERNEL_SOURCES = {"serial": _FWD_SOURCES,
+                  "segment": _FWD_SOURCES + ["chunked_kda_delta_gb300/csrc/kda_merge.cu"]}
+KERNEL_NAMES = {"serial": "kda_fwd_tc_kernel",
+                "segment": "kda_fwd_tc_kernel x3 + kda_merge_kernel (whole step)"}
+LAUNCHES_PER_STEP = {"serial": 1, "segment": 4}
 
 
 def parse_args():
@@ -280,6 +288,8 @@ def workload_config(w, args, note=None):
                                             f"{w.num_seqs} sequences, {w.total_tokens} tokens"),
            "num_heads": w.num_heads, "head_dim": 128, "chunk": 16,
            "initial_state": w.has_initial_state, "final_state": True, "mode": args.mode,
+           "segment_len": (args.segment_len or 8192) if args.mode == "segment" else None,
+           "precision": "bf16 tensor-core operands, fp32 accumulation, fp32 state",
            "head_tokens_per_gpu": w.head_tokens, "parallelism": f"replicas x{args.gpus}",
            "l2": "no flush; inputs larger than L2 "
                  f"({algorithmic_bytes(w) / 1e6:.0f} MB per step vs 129 MB)"}
@@ -327,7 +337,11 @@ def main():
     torch.cuda.synchronize()
     if K.kda_get_device_status() != 0:
         raise RuntimeError("device status error after warm-up")
-    launches_per_step = 1
+    launches_per_step = LAUNCHES_PER_STEP[args.mode]
+    if args.mode == "segment":
+        seg = args.segment_len or 8192
+        if w.dense and w.seq_lens[0] <= seg:
+            launches_per_step = 1  # a single segment runs the plain serial pass
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
