@@ -283,6 +283,21 @@ def run_reference(args, w):
     }))
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings (identity without a process group)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(world: int, head_tokens_per_rank: int, steps: int, seconds: float) -> float:
+    """Whole-job head-tokens/s: every rank runs its own copy of the workload (weak scaling)."""
+    return world * head_tokens_per_rank * steps / seconds
+
+
 def workload_config(w, args, note=None):
     cfg = {"workload": w.name, "seq_lens": (list(w.seq_lens) if len(w.seq_lens) <= 4 else
                                             f"{w.num_seqs} sequences, {w.total_tokens} tokens"),
@@ -363,11 +378,8 @@ def main():
     kernel_ms = statistics.mean(s.elapsed_time(e) for s, e in evs)
     if K.kda_get_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
-    if pg:
-        t = torch.tensor([elapsed_ms, kernel_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms, kernel_ms = float(t[0]), float(t[1])
-    value = world * w.head_tokens * args.steps / (elapsed_ms / 1e3)
+    elapsed_ms, kernel_ms = max_over_ranks([elapsed_ms, kernel_ms], pg, dev)
+    value = job_throughput(world, w.head_tokens, args.steps, elapsed_ms / 1e3)
 
     e2e = None
     if not args.no_e2e:
@@ -392,15 +404,12 @@ def main():
         for _ in range(args.e2e_steps):
             e2e_step()
         e2e_s = (time.perf_counter() - t) / args.e2e_steps
-        if pg:
-            tt = torch.tensor([e2e_s], device=dev)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            e2e_s = float(tt[0])
+        e2e_s = max_over_ranks([e2e_s], pg, dev)[0]
         h2d = sum(x.numel() * x.element_size() for x in host.values())
         h2d += 0 if s0h is None else s0h.numel() * 4
         h2d += 0 if cuh is None else cuh.numel() * 4
         d2h = oh.numel() * 2 + fh.numel() * 4
-        e2e = {"value": world * w.head_tokens / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_throughput(world, w.head_tokens, 1, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
 
     cpu = None
