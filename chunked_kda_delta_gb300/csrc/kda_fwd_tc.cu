@@ -110,8 +110,10 @@ constexpr int kSmemBytes = kSmFail + 4 * kK1Groups;
 static_assert(kSmOTile + 2 * kOTileBytes <= kSmBar, "K2 buffers overlap the barriers");
 static_assert(kSmOTile % 128 == 0, "TMA store source must be 128-byte aligned");
 enum {  // K1 CTA barriers
-    BAR_IN_FULL = 0, BAR_IN_EMPTY = 4, BAR_OUT_FREE = 8
+    BAR_IN_FULL = 0, BAR_IN_EMPTY = 4, BAR_OUT_FREE = 8,
+    BAR_COPIED = BAR_OUT_FREE + kRecvStages  // per K1 group: its last bulk copy has landed
 };
+static_assert(BAR_COPIED + kK1Groups <= kNumBars, "too many barriers");
 enum {  // K2 CTA barriers
     BAR_K1_FULL = 0, BAR_D1 = 3, BAR_SDONE = 4, BAR_DRAIN = 5, BAR_NEVER = 6
 };
@@ -183,6 +185,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mbar_init(bar(BAR_IN_EMPTY + s), 1);
             }
             for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_OUT_FREE + s), 8);
+            for (int gi = 0; gi < kK1Groups; ++gi) mbar_init(bar(BAR_COPIED + gi), 1);
             for (int gi = 0; gi < kK1Groups; ++gi) fail_flag[gi] = 0;
         } else {
             for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_K1_FULL + s), 1);
@@ -269,10 +272,16 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const bool with_out = (p.flags & kFlagNoOutput) == 0;
         for (int c = gi; c < nchunks; c += kK1Groups) {
             const int s = c % kInStages;
-            bool ok = mbar_wait(bar(BAR_IN_FULL + s), (c / kInStages) & 1, lim) && !fail_flag[gi];
-            // The local operand buffer is rewritten below: the previous copy out of it
-            // must have finished reading.
-            if (kt == 0 && c >= kK1Groups) bulk_wait_read0();
+            // One thread waits for the input tiles and for the landing of the group's
+            // previous bulk copy (its local operand buffer is rewritten below: a copy into
+            // the peer CTA completes only through the peer's barrier, which the K2 CTA
+            // relays back); the group barrier then publishes both to the group.
+            bool ok = !fail_flag[gi];
+            if (kt == 0) {
+                ok = ok && mbar_wait(bar(BAR_IN_FULL + s), (c / kInStages) & 1, lim);
+                if (c >= kK1Groups)
+                    ok = ok && mbar_wait(bar(BAR_COPIED + gi), ((c / kK1Groups) - 1) & 1, lim);
+            }
             if (named_bar_or(nbar, 128, !ok)) {
                 if (kt == 0) record(p.status, kStatusTimeout);
                 break;
@@ -360,28 +369,29 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int r = g + 8 * (e >> 1), sc = 8 * nt + 2 * t + (e & 1);
-                            Asm[r * 16 + sc] = sc < r ? bet[r] * acc[nt][e] : 0.f;
+                            Asm[sc * 16 + r] = sc < r ? bet[r] * acc[nt][e] : 0.f;  // A^T
                         }
                     __syncwarp();
                     if (lane < 16) {
-                        // Column sc of T = (I + A)^{-1}: x_r = [r == sc] - sum_{m<r} A[r][m] x_m.
+                        // Column sc of T = (I + A)^{-1} by right-looking forward substitution:
+                        // once x_m is final, x_r -= A[r][m] x_m for every r > m.  The updates
+                        // of one step are independent, so the dependent chain is 15 FMAs.
                         const int sc = lane;
                         float x[kChunk];
 #pragma unroll
-                        for (int r = 0; r < kChunk; ++r) {
-                            float a = 0.f;
-                            const float4* arow = reinterpret_cast<const float4*>(Asm + r * 16);
+                        for (int r = 0; r < kChunk; ++r) x[r] = r == sc ? 1.f : 0.f;
 #pragma unroll
-                            for (int m4 = 0; m4 < 4; ++m4) {
-                                if (4 * m4 < r) {
-                                    const float4 av = arow[m4];
-                                    if (4 * m4 + 0 < r) a = fmaf(av.x, x[4 * m4 + 0], a);
-                                    if (4 * m4 + 1 < r) a = fmaf(av.y, x[4 * m4 + 1], a);
-                                    if (4 * m4 + 2 < r) a = fmaf(av.z, x[4 * m4 + 2], a);
-                                    if (4 * m4 + 3 < r) a = fmaf(av.w, x[4 * m4 + 3], a);
-                                }
+                        for (int m = 0; m < kChunk - 1; ++m) {
+                            const float xm = x[m];
+                            const float4* acol = reinterpret_cast<const float4*>(Asm + m * 16);
+#pragma unroll
+                            for (int r4 = (m + 1) >> 2; r4 < 4; ++r4) {
+                                const float4 av = acol[r4];
+                                if (4 * r4 + 0 > m) x[4 * r4 + 0] = fmaf(-av.x, xm, x[4 * r4 + 0]);
+                                if (4 * r4 + 1 > m) x[4 * r4 + 1] = fmaf(-av.y, xm, x[4 * r4 + 1]);
+                                if (4 * r4 + 2 > m) x[4 * r4 + 2] = fmaf(-av.z, xm, x[4 * r4 + 2]);
+                                if (4 * r4 + 3 > m) x[4 * r4 + 3] = fmaf(-av.w, xm, x[4 * r4 + 3]);
                             }
-                            x[r] = r < sc ? 0.f : (r == sc ? 1.f : -a);
                         }
                         const float bs = bet[sc];
 #pragma unroll
@@ -467,7 +477,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                mbar_wait_cluster(bar(BAR_OUT_FREE + os), ((c / kRecvStages) - 1) & 1, lim);
                 if (free_ok) {
                     const uint32_t rbar = mapa(bar(BAR_K1_FULL + os), 1);
-                    mbar_arrive_expect_tx_remote(rbar, (uint32_t)kOutBytes);
+                    mbar_arrive_expect_tx_remote_relaxed(rbar, (uint32_t)kOutBytes);
                     bulk_copy_to_peer(mapa(sbase + kSmRecv + os * kOutBytes, 1), smem_u32(ob),
                                       (uint32_t)kOutBytes, rbar);
                     bulk_commit();
@@ -476,10 +486,24 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
         }
-        if (kt == 0) bulk_wait0();  // every copy into the peer completed before exit
-    } else if (warp == 0 || warp > 8) {
+        // Copies still in flight at exit land before the K2 CTA reaches the final
+        // cluster barrier (it waits for every chunk), so this CTA's memory stays valid.
+    } else if (warp == 0 || warp > 9) {
         // TMEM owner (warp 0): allocated above, released after the final barrier.
-        // Warps 9+ of the K2 CTA exist because both CTAs share one block size.
+        // Warps 10+ of the K2 CTA exist because both CTAs share one block size.
+    } else if (warp == 9) {
+        // Copy relay: tells each K1 group when its bulk copy has landed, so that it may
+        // rewrite the local buffer the copy read from.
+        if (lane == 0) {
+            for (int c = 0; c < nchunks; ++c) {
+                if (!mbar_wait(bar(BAR_K1_FULL + c % kRecvStages), (c / kRecvStages) & 1, lim)) {
+                    record(p.status, kStatusTimeout);
+                    break;
+                }
+                mbar_arrive_remote_relaxed(mapa(bar(BAR_COPIED + c % kK1Groups), 0));
+            }
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ K2 state chain (256 threads)
         const int quad = warp & 3;                 // TMEM lane quadrant = SM sub-partition
@@ -575,7 +599,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int c = 0; ok && c < nchunks; ++c) {
             const int ks = c % kRecvStages;
             const uint32_t ob = sbase + kSmRecv + ks * kOutBytes;
-            bool w = mbar_wait_cluster(bar(BAR_K1_FULL + ks), (c / kRecvStages) & 1, lim);
+            bool w = mbar_wait(bar(BAR_K1_FULL + ks), (c / kRecvStages) & 1, lim);
             if (c > 0) w = w && mbar_wait(bar(BAR_SDONE), (c - 1) & 1, lim);
             // The tile being refilled this iteration (chunk c-1's buffer, last stored from
             // chunk c-3) must have been read by its TMA store.

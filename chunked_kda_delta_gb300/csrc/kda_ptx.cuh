@@ -92,6 +92,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cbar, uint
                  "r"(bytes)
                  : "memory");
 }
+// Arrive on a peer CTA's barrier announcing `bytes` of incoming bulk-copy data.  The
+// data itself completes the transaction count, so the arrive needs no release ordering.
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote_relaxed(uint32_t cbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar),
+                 "r"(bytes)
+                 : "memory");
+}
 // Relaxed arrive on a peer CTA's barrier: for "done reading" signals whose reads have
 // already been consumed (no release ordering of earlier stores is needed).
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cbar) {
@@ -234,6 +241,13 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                  : KDA_R8(r, 0)
                  : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : KDA_R8(r, 0), KDA_R8(r, 8)
+        : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -290,6 +304,11 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                                           uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
                  : "r"(addr));
 }
 // D(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col)
