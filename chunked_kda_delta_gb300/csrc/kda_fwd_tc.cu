@@ -70,10 +70,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 // TMEM column map (K2 CTA)
 constexpr uint32_t kColS = 0;     // S^T fp32, 128 columns
 constexpr uint32_t kColSA = 128;  // S^T bf16 pairs, 64 columns (MMA1 A operand)
-// MMA1 accumulators: 2 buffers x 4 K-quarter partials x 32 columns; in each partial,
-// columns 0-15 hold S^T W^T and 16-31 hold S^T Qtil^T (+ delta^T Mq^T in partial 0).
+// MMA1 accumulators: 2 buffers x 2 K-half partials x 32 columns; in each partial,
+// columns 0-15 hold D^T W^T and 16-31 hold D^T Qtil^T; partial 0 also collects the
+// lookahead terms delta^T [P ; R]^T of the previous chunk and delta^T Mq^T.
 constexpr uint32_t kColD1 = 192;
-constexpr uint32_t kColDA = 448;  // delta^T bf16 pairs, 8 columns (MMA2/MMA3 A operand)
+constexpr uint32_t kD1Buf = 64;   // columns per MMA1 buffer
+constexpr uint32_t kColDA = 320;  // 2 buffers x 8 columns: delta^T bf16 pairs (A operand)
 
 // Input stage (K1 CTA): q, k, v bf16 [16][128]; g fp32 [16][128]; beta fp32 [16].
 constexpr int kInQ = 0, kInK = 4096, kInV = 8192, kInG = 12288, kInBeta = 20480;
@@ -87,7 +89,10 @@ constexpr uint32_t kTxBytes = 20480;  // q, k, v, g tiles
 constexpr int kURow = 132;
 constexpr int kB1 = 0, kB2 = 8192, kB3 = 12288, kU = 12800, kGC = kU + 16 * kURow * 4,
               kOutBytes = kGC + 512;
-constexpr int kRecvStages = 3;
+// Receive ring: two stages per K1 group (chunk c -> stage c % 6, group c % 3), so a stage
+// is only refilled by the group that filled it last and its release barrier is never
+// more than one phase behind that group.
+constexpr int kRecvStages = 2 * kK1Groups;
 constexpr uint32_t kLbo = 128, kSboB1 = 2048, kSboB2 = 256, kSboB3 = 256;
 // K1 group scratch: padded bf16 staging rows (136 elements), exp(gam_ref), A, Tb, beta.
 constexpr int kStRow = 272, kStArr = 16 * kStRow;
@@ -102,12 +107,19 @@ constexpr int kSmOutLocal = kSmGrp + kK1Groups * kGrpBytes;
 constexpr int kSmRecv = 0;
 constexpr int kSmOTile = kSmRecv + kRecvStages * kOutBytes;  // K2 CTA: 2 output tiles bf16 [16][128]
 constexpr int kOTileBytes = kChunk * kD * 2;
+constexpr int kOTiles = 4;  // output tiles: a tile is rewritten 4 chunks after its store
+// K2 CTA: ring of [P ; R] lookahead operands (bf16, N = 32 x K = 16, K-major):
+// P_c = W_{c+1} Kbar_c^T, R_c = Qtil_{c+1} Kbar_c^T.
+constexpr int kSmPR = kSmOTile + kOTiles * kOTileBytes;
+constexpr int kPRBytes = 1024;
+constexpr int kPRSlots = 3;
 constexpr int kSmBar = kSmOutLocal + kK1Groups * kOutBytes;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 24;
 constexpr int kSmTmemSlot = kSmBar + kNumBars * 8;
 constexpr int kSmFail = kSmTmemSlot + 8;            // int32 per K1 group: failure flags
-constexpr int kSmemBytes = kSmFail + 4 * kK1Groups;
-static_assert(kSmOTile + 2 * kOTileBytes <= kSmBar, "K2 buffers overlap the barriers");
+constexpr int kSmK2Fail = kSmFail + 4 * kK1Groups;  // int32: K2 CTA failure flag
+constexpr int kSmemBytes = kSmK2Fail + 4;
+static_assert(kSmPR + kPRSlots * kPRBytes <= kSmBar, "K2 buffers overlap the barriers");
 static_assert(kSmOTile % 128 == 0, "TMA store source must be 128-byte aligned");
 enum {  // K1 CTA barriers
     BAR_IN_FULL = 0, BAR_IN_EMPTY = 4, BAR_OUT_FREE = 8,
@@ -115,9 +127,21 @@ enum {  // K1 CTA barriers
 };
 static_assert(BAR_COPIED + kK1Groups <= kNumBars, "too many barriers");
 enum {  // K2 CTA barriers
-    BAR_K1_FULL = 0, BAR_D1 = 3, BAR_SDONE = 4, BAR_DRAIN = 5, BAR_NEVER = 6
+    BAR_K1_FULL = 0,                       // kRecvStages: chunk operands landed
+    BAR_D1 = BAR_K1_FULL + kRecvStages,    // MMA1 group of a chunk complete (2 commits)
+    BAR_SDONE,                             // state update and Mq delta complete (1 commit)
+    BAR_DRAIN,                             // every MMA complete before exit (3 issuers)
+    BAR_NEVER,                             // never signalled (timeout-path test)
+    BAR_PR_FULL,                           // kPRSlots: [P ; R] operand written
+    BAR_PR_FREE = BAR_PR_FULL + kPRSlots,  // kPRSlots: [P ; R] operand consumed
+    BAR_K2_END = BAR_PR_FREE + kPRSlots
 };
-constexpr uint32_t kNamedK2 = 1 + kK1Groups;  // K1 groups use named barriers 1 .. kK1Groups
+static_assert(BAR_K2_END <= kNumBars, "too many barriers");
+// K2 CTA named barriers (the K1 CTA uses 1 .. kK1Groups in its own CTA): the state
+// chain (8 warps) arrives, the MMA issuers wait.
+constexpr uint32_t kNamedIssue = 1;  // delta_c and D_{c+1} written: state update, Mq
+constexpr uint32_t kNamedEmit = 2;   // output of chunk c-1 read, bf16 D_{c+1} written: MMA1(c+1)
+constexpr uint32_t kChainThreads = 256, kIssueCount = kChainThreads + 32, kEmitCount = kChainThreads + 64;
 
 __device__ __forceinline__ uint32_t b1_off(int n, int k) {
     return (n >> 3) * kSboB1 + (k >> 3) * kLbo + (n & 7) * 16 + (k & 7) * 2;
@@ -184,15 +208,20 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mbar_init(bar(BAR_IN_FULL + s), 1);
                 mbar_init(bar(BAR_IN_EMPTY + s), 1);
             }
-            for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_OUT_FREE + s), 8);
+            for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_OUT_FREE + s), 1);
             for (int gi = 0; gi < kK1Groups; ++gi) mbar_init(bar(BAR_COPIED + gi), 1);
             for (int gi = 0; gi < kK1Groups; ++gi) fail_flag[gi] = 0;
         } else {
             for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_K1_FULL + s), 1);
-            mbar_init(bar(BAR_D1), 4);     // one commit per MMA1 slice (K-quarter)
-            mbar_init(bar(BAR_SDONE), 2);  // the state update and Mq delta
-            mbar_init(bar(BAR_DRAIN), 8);
-            mbar_init(bar(BAR_NEVER), 1);  // never signalled (timeout-path test)
+            mbar_init(bar(BAR_D1), 2);
+            mbar_init(bar(BAR_SDONE), 1);
+            mbar_init(bar(BAR_DRAIN), 3);
+            *reinterpret_cast<volatile int32_t*>(smem + kSmK2Fail) = 0;
+            mbar_init(bar(BAR_NEVER), 1);
+            for (int s = 0; s < kPRSlots; ++s) {
+                mbar_init(bar(BAR_PR_FULL + s), 1);
+                mbar_init(bar(BAR_PR_FREE + s), 1);
+            }
         }
         fence_mbar_init();
     }
@@ -488,243 +517,354 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         // Copies still in flight at exit land before the K2 CTA reaches the final
         // cluster barrier (it waits for every chunk), so this CTA's memory stays valid.
-    } else if (warp == 0 || warp > 9) {
-        // TMEM owner (warp 0): allocated above, released after the final barrier.
-        // Warps 10+ of the K2 CTA exist because both CTAs share one block size.
-    } else if (warp == 9) {
-        // Copy relay: tells each K1 group when its bulk copy has landed, so that it may
-        // rewrite the local buffer the copy read from.
-        if (lane == 0) {
-            for (int c = 0; c < nchunks; ++c) {
-                if (!mbar_wait(bar(BAR_K1_FULL + c % kRecvStages), (c / kRecvStages) & 1, lim)) {
-                    record(p.status, kStatusTimeout);
-                    break;
-                }
-                mbar_arrive_remote_relaxed(mapa(bar(BAR_COPIED + c % kK1Groups), 0));
-            }
-        }
-        __syncwarp();
     } else {
-        // ------------------------------------------------------------ K2 state chain (256 threads)
-        const int quad = warp & 3;                 // TMEM lane quadrant = SM sub-partition
-        const int hf = (warp - 1) >> 2;            // 0: key columns 0-63, 1: 64-127
-        const int j = 32 * quad + lane;            // value column owned by this thread
-        const uint32_t lanes = (uint32_t)(32 * quad) << 16;
-        const uint32_t tS = tmem + lanes + kColS + 64u * hf;
-        const uint32_t tSA = tmem + lanes + kColSA + 32u * hf;
-        const uint32_t tDA = tmem + lanes + kColDA + 4u * hf;
+        // ------------------------------------------------------------ K2 CTA
+        // Chunk c, with D_c = Diag(exp gam_C(c-1)) S_{c-1} (D_0 = S_0):
+        //   W_c S_c = W_c D_c + P_{c-1} delta_{c-1},  P_{c-1} = W_c Kbar_{c-1}^T (likewise Qtil, R)
+        // so the products of chunk c with the state (MMA1) run on D_c, which exists before
+        // delta_{c-1} does.  Roles (all hand-offs are mbarriers or arrive/wait named barriers,
+        // so no warp waits for another's unrelated work):
+        //   warps 1-8   state chain: D_{c+1} = decay of S_c (fp32, and its bf16 copy),
+        //               delta_c, then the output of chunk c-1;
+        //   warp 11     S += Kbar_c^T delta_c and the Mq delta_c output term (after delta_c);
+        //   warps 12, 0 MMA1(c+1) over the two K halves, plus the lookahead term
+        //               delta_c [P_c ; R_c]^T (after the output of chunk c-1 was read);
+        //               warp 12 also issues the output tiles' TMA stores;
+        //   warp 10     [P_c ; R_c] with mma.sync, ahead of the chain;
+        //   warp 9      tells each K1 group when its bulk copy has landed.
+        volatile int32_t* k2fail = reinterpret_cast<volatile int32_t*>(smem + kSmK2Fail);
+        const bool with_out = (p.flags & kFlagNoOutput) == 0;
         const uint32_t idesc32 = idesc_bf16(128, 32), idesc128 = idesc_bf16(128, 128),
                        idesc16 = idesc_bf16(128, 16);
-        const bool with_out = (p.flags & kFlagNoOutput) == 0;
-        const bool store_issuer = warp == 1;       // issues (and drains) the TMA stores
-        // State rows: initial state at this CTA's row; final state at its row, or (segment
-        // runs) at sequence b for the last segment only.
-        const size_t soff = ((size_t)n * p.H + h) * kD * kD;
-        size_t foff = soff;
-        bool write_final = p.sfin != nullptr;
-        if (p.flags & kFlagFinalLastSeg) {
-            const int b = n / p.nseg_used, sg = n % p.nseg_used;
-            write_final = write_final && sg == p.nseg_total - 1;
-            foff = ((size_t)b * p.H + h) * kD * kD;
-        }
-        uint32_t sreg[64];
-        // Initial state S0[i][j] for keys i of this half -> S^T[j][i].
-        if (p.flags & kFlagIdentityS0) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) sreg[i] = (64 * hf + i == j) ? __float_as_uint(1.f) : 0u;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-                sreg[i] = p.s0 ? __float_as_uint(p.s0[soff + (size_t)(64 * hf + i) * kD + j]) : 0u;
-        }
-        tmem_st32(tS, sreg);
-        tmem_st32(tS + 32, sreg + 32);
-        tmem_wait_st();
-        // Sum over the 4 K-quarter partials of 8 accumulator columns (rows 8hf..8hf+7);
-        // `col` selects the S^T W^T (0) or the output (16) half of each partial.
-        auto ld_partials = [&](uint32_t buf, uint32_t col, float (&v)[8]) {
-            uint32_t a[8], b[8], c2[8], d[8];
-            const uint32_t base = tmem + lanes + kColD1 + 128u * buf + col + 8 * hf;
-            tmem_ld8(base, a);
-            tmem_ld8(base + 32, b);
-            tmem_ld8(base + 64, c2);
-            tmem_ld8(base + 96, d);
-            tmem_wait_ld_regs<8>(a);
-            tmem_wait_ld_regs<8>(b);
-            tmem_wait_ld_regs<8>(c2);
-            tmem_wait_ld_regs<8>(d);
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-                v[r] = (__uint_as_float(a[r]) + __uint_as_float(b[r])) +
-                       (__uint_as_float(c2[r]) + __uint_as_float(d[r]));
+        const uint32_t idesc1 = with_out ? idesc32 : idesc16;  // MMA1 N: W and Qtil, or W only
+        auto k1_full = [&](int c) {
+            return mbar_wait(bar(BAR_K1_FULL + c % kRecvStages), (c / kRecvStages) & 1, lim);
         };
-        // Output rows of chunk cp: a full chunk goes through a shared-memory tile and one
-        // TMA store (issued after the next K2 barrier); the ragged last chunk of a
-        // sequence is written with plain stores so that no row past the sequence is
-        // touched.  Returns true when a tile was filled.
-        auto emit_out = [&](int cp) -> bool {
-            const int64_t t0p = bos + (int64_t)cp * kChunk;
-            const int Cp = (eos - t0p < kChunk) ? (int)(eos - t0p) : kChunk;
-            float o[8];
-            ld_partials(cp & 1, 16, o);
-            if (Cp == kChunk) {
-                __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem + kSmOTile + (cp & 1) * kOTileBytes);
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    tile[(8 * hf + r) * kD + j] = __float2bfloat16_rn(p.scale * o[r]);
-                fence_proxy_async_smem();
-                return true;
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int row = 8 * hf + r;
-                if (row < Cp)
-                    p.out[((t0p + row) * H + h) * kD + j] = __float2bfloat16_rn(p.scale * o[r]);
-            }
-            return false;
-        };
-        int tile_pending = -1;  // chunk whose tile awaits its TMA store
-        auto issue_tile_store = [&]() {
-            if (tile_pending >= 0 && store_issuer && elect_one()) {
-                const int32_t t0p = (int32_t)(bos + (int64_t)tile_pending * kChunk);
-                tma_store_3d(&tm_out, sbase + kSmOTile + (tile_pending & 1) * kOTileBytes, 0, h, t0p);
-                bulk_commit();
+        auto stage = [&](int c) { return sbase + kSmRecv + (uint32_t)(c % kRecvStages) * kOutBytes; };
+        if ((p.debug_flags & 1) && !mbar_wait(bar(BAR_NEVER), 0, lim)) *k2fail = 1;  // never signalled
+
+        if (warp == 9) {
+            // ---- copy relay
+            if (lane == 0) {
+                for (int c = 0; c < nchunks; ++c) {
+                    if (!k1_full(c)) {
+                        record(p.status, kStatusTimeout);
+                        break;
+                    }
+                    mbar_arrive_remote_relaxed(mapa(bar(BAR_COPIED + c % kK1Groups), 0));
+                }
             }
             __syncwarp();
-            tile_pending = -1;
-        };
-        bool ok = true;
-        if (p.debug_flags & 1) ok = mbar_wait(bar(BAR_NEVER), 0, lim);  // nothing signals it
-        if (named_bar_or(kNamedK2, 256, !ok)) ok = false;
-        for (int c = 0; ok && c < nchunks; ++c) {
-            const int ks = c % kRecvStages;
-            const uint32_t ob = sbase + kSmRecv + ks * kOutBytes;
-            bool w = mbar_wait(bar(BAR_K1_FULL + ks), (c / kRecvStages) & 1, lim);
-            if (c > 0) w = w && mbar_wait(bar(BAR_SDONE), (c - 1) & 1, lim);
-            // The tile being refilled this iteration (chunk c-1's buffer, last stored from
-            // chunk c-3) must have been read by its TMA store.
-            if (store_issuer && lane == 0) bulk_wait_read0();
-            if (named_bar_or(kNamedK2, 256, !w)) { ok = false; break; }
-            tc_fence_after();
-            issue_tile_store();
-            // The previous chunk's stage is no longer read (its U and exp(gam_C) were
-            // consumed last iteration; the MMAs reading B1..B3 completed): hand it back.
-            if (c > 0 && lane == 0)
-                mbar_arrive_remote_relaxed(mapa(bar(BAR_OUT_FREE + (c - 1) % kRecvStages), 0));
-            // (A) S_c (this half) -> bf16 copy for MMA1
-            tmem_ld32(tS, sreg);
-            tmem_ld32(tS + 32, sreg + 32);
-            tmem_wait_ld_regs<64>(sreg);
+        } else if (warp == 10) {
+            // ---- [P_m ; R_m] = [W_{m+1} ; Qtil_{m+1}] Kbar_m^T (16x16 each, K = 128)
+            for (int m = 0; m + 1 < nchunks; ++m) {
+                const int slot = m % kPRSlots;
+                bool w = !*k2fail;
+                if (w && m >= kPRSlots) w = mbar_wait(bar(BAR_PR_FREE + slot), ((m / kPRSlots) - 1) & 1, lim);
+                w = w && k1_full(m) && k1_full(m + 1);
+                if (__any_sync(0xffffffffu, !w)) {
+                    if (lane == 0) record(p.status, kStatusTimeout);
+                    break;
+                }
+            const uint32_t b1 = sbase + kSmRecv + ((m + 1) % kRecvStages) * kOutBytes + kB1;
+            const uint32_t b2 = sbase + kSmRecv + (m % kRecvStages) * kOutBytes + kB2;
+            float acc[2][2][2][4];  // [P or R][8-column tile][k parity][fragment]
+#pragma unroll
+            for (int a0 = 0; a0 < 2; ++a0)
+#pragma unroll
+                for (int a1 = 0; a1 < 2; ++a1)
+#pragma unroll
+                    for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[a0][a1][a2][e] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int i0 = 16 * kk;
+                // B fragments of both 8-column tiles: Kbar rows s, channels i0 .. i0+15
+                uint32_t bf[4];
+                ldsm_x4_t(b2 + ((i0 + 8 * ((lane >> 3) & 1) + (lane & 7)) >> 3) * kSboB2 +
+                              (lane >> 4) * kLbo + (lane & 7) * 16,
+                          bf[0], bf[1], bf[2], bf[3]);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    if (mt == 1 && !with_out) continue;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(b1 + b1_off(16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1), i0 + 8 * (lane >> 4)),
+                            a0, a1, a2, a3);
+                    mma_16816(acc[mt][0][kk & 1], a0, a1, a2, a3, bf[0], bf[1]);
+                    mma_16816(acc[mt][1][kk & 1], a0, a1, a2, a3, bf[2], bf[3]);
+                }
+            }
+            unsigned char* prp = smem + kSmPR + slot * kPRBytes;
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const float* x0 = acc[mt][nt][0];
+                    const float* x1 = acc[mt][nt][1];
+                    const int sc = 8 * nt + 2 * t;
+                    *reinterpret_cast<uint32_t*>(prp + mt * 512 + b3_off(g, sc)) =
+                        pack_bf16(x0[0] + x1[0], x0[1] + x1[1]);
+                    *reinterpret_cast<uint32_t*>(prp + mt * 512 + b3_off(g + 8, sc)) =
+                        pack_bf16(x0[2] + x1[2], x0[3] + x1[3]);
+                }
+            fence_proxy_async_smem();
+            __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_PR_FULL + slot));
+            }
+        } else if (warp == 11) {
+            // ---- state update and Mq delta
+            // Every iteration commits, with or without MMAs: after a failure the commits
+            // still pace the chain one generation at a time.
+            for (int c = 0; c < nchunks; ++c) {
+                named_bar_sync(kNamedIssue, kIssueCount);
+                const bool live = !*k2fail;
+                tc_fence_after();
+                if (elect_one()) {
+                    if (live) {
+                        const uint32_t da = tmem + kColDA + 8u * (c & 1);
+                        mma_ts(tmem + kColS, da, sdesc(stage(c) + kB2, kLbo, kSboB2), idesc128, 1);
+                        if (with_out)
+                            mma_ts(tmem + kColD1 + kD1Buf * (c & 1) + 16, da, sdesc(stage(c) + kB3, kLbo, kSboB3),
+                                   idesc16, 1);
+                    }
+                    tc_commit(bar(BAR_SDONE));
+                }
+                __syncwarp();
+                // Chunk c-1's stage is no longer read (its last MMAs completed before the
+                // chain reached this point): hand it back to the K1 CTA.
+                if (live && c > 0 && lane == 0)
+                    mbar_arrive_remote_relaxed(mapa(bar(BAR_OUT_FREE + (c - 1) % kRecvStages), 0));
+            }
+        } else if (warp == 12 || warp == 0) {
+            // ---- MMA1 over K half `kh` (warp 12: keys 0-63 plus the lookahead term)
+            const int kh = warp == 12 ? 0 : 1;
+            auto mma1 = [&](int c) {
+                const uint32_t d = tmem + kColD1 + kD1Buf * (c & 1) + 32u * kh;
+                const uint32_t b1 = stage(c) + kB1;
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const int kk = 4 * kh + s4;
+                    mma_ts(d, tmem + kColSA + 8u * kk, sdesc(b1 + kk * 2 * kLbo, kLbo, kSboB1), idesc1, s4);
+                }
+                if (kh == 0 && c > 0)
+                    mma_ts(d, tmem + kColDA + 8u * ((c - 1) & 1),
+                           sdesc(sbase + kSmPR + ((c - 1) % kPRSlots) * kPRBytes, kLbo, kSboB3), idesc1, 1);
+                tc_commit(bar(BAR_D1));
+            };
+            // EMIT(-1): S_0 and its bf16 copy written
+            // Every chunk's MMA1 commit happens, with or without MMAs (see warp 11).
+            named_bar_sync(kNamedEmit, kEmitCount);
+            if (nchunks > 0) {
+                const bool live = !*k2fail && __all_sync(0xffffffffu, k1_full(0));
+                if (!live && lane == 0) *k2fail = 1;
+                tc_fence_after();
+                if (elect_one()) {
+                    if (live) mma1(0);
+                    else tc_commit(bar(BAR_D1));
+                }
+                __syncwarp();
+            }
+            for (int c = 0; c < nchunks; ++c) {
+                named_bar_sync(kNamedEmit, kEmitCount);  // EMIT(c)
+                bool live = !*k2fail;
+                tc_fence_after();
+                if (live && kh == 0 && c > 0 && with_out && lane == 0) {
+                    // output tile of chunk c-1 (written by the chain before EMIT(c)); the
+                    // chain refills a tile only after MMA1(c+1), so after this wait the
+                    // store of chunk c-4 (same tile as chunk c) has read its source
+                    const int32_t t0p = (int32_t)(bos + (int64_t)(c - 1) * kChunk);
+                    tma_store_3d(&tm_out, sbase + kSmOTile + ((c - 1) % kOTiles) * kOTileBytes, 0, h, t0p);
+                    bulk_commit();
+                    bulk_wait_read<2>();
+                }
+                __syncwarp();
+                if (c + 1 < nchunks) {
+                    if (live) {
+                        bool v = k1_full(c + 1);
+                        if (kh == 0) v = v && mbar_wait(bar(BAR_PR_FULL + c % kPRSlots), (c / kPRSlots) & 1, lim);
+                        live = __all_sync(0xffffffffu, v);
+                        if (!live && lane == 0) *k2fail = 1;
+                    }
+                    if (elect_one()) {
+                        if (live) mma1(c + 1);
+                        else tc_commit(bar(BAR_D1));
+                    }
+                    __syncwarp();
+                }
+            }
+            if (kh == 0 && lane == 0) bulk_wait0();  // TMA stores complete before exit
+        } else {
+            // ---- state chain (warps 1-8, 256 threads)
+            const int quad = warp & 3;                 // TMEM lane quadrant = SM sub-partition
+            const int hf = (warp - 1) >> 2;            // key columns 64hf.., delta rows 8hf..
+            const int j = 32 * quad + lane;            // value column owned by this thread
+            const uint32_t lanes = (uint32_t)(32 * quad) << 16;
+            const uint32_t tS = tmem + lanes + kColS + 64u * hf;
+            const uint32_t tSA = tmem + lanes + kColSA + 32u * hf;
+            // State rows: initial state at this CTA's row; final state at its row, or (segment
+            // runs) at sequence b for the last segment only.
+            const size_t soff = ((size_t)n * p.H + h) * kD * kD;
+            size_t foff = soff;
+            bool write_final = p.sfin != nullptr;
+            if (p.flags & kFlagFinalLastSeg) {
+                const int b = n / p.nseg_used, sg = n % p.nseg_used;
+                write_final = write_final && sg == p.nseg_total - 1;
+                foff = ((size_t)b * p.H + h) * kD * kD;
+            }
+            uint32_t sreg[64];
+            // Initial state S0[i][j] for keys i of this half -> S^T[j][i], and its bf16 copy.
+            if (p.flags & kFlagIdentityS0) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) sreg[i] = (64 * hf + i == j) ? __float_as_uint(1.f) : 0u;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    sreg[i] = p.s0 ? __float_as_uint(p.s0[soff + (size_t)(64 * hf + i) * kD + j]) : 0u;
+            }
+            tmem_st32(tS, sreg);
+            tmem_st32(tS + 32, sreg + 32);
             {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     pk[i] = pack_bf16(__uint_as_float(sreg[2 * i]), __uint_as_float(sreg[2 * i + 1]));
                 tmem_st32(tSA, pk);
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            named_bar_sync(kNamedK2, 256);
-            tc_fence_after();
-            // MMA1 slice: warps of half 0 take K-quarter `quad`; N = 32 covers W and Qtil
-            // (only W without output rows).
-            if (hf == 0) {
-                if (elect_one()) {
-                    const uint32_t d = tmem + kColD1 + 128u * (c & 1) + 32u * quad;
-#pragma unroll
-                    for (int s2 = 0; s2 < 2; ++s2) {
-                        const int kk = 2 * quad + s2;
-                        mma_ts(d, tmem + kColSA + 8u * kk,
-                               sdesc(ob + kB1 + kk * 2 * kLbo, kLbo, kSboB1),
-                               with_out ? idesc32 : idesc16, s2);
-                    }
-                    tc_commit(bar(BAR_D1));
-                }
-                __syncwarp();
-            }
-            // (D) decay S by exp(gam_C) ahead of the state update
-            {
-                const float4* gc4 = reinterpret_cast<const float4*>(smem + kSmRecv + ks * kOutBytes + kGC) + 16 * hf;
-#pragma unroll
-                for (int i4 = 0; i4 < 16; ++i4) {
-                    const float4 gv = gc4[i4];
-                    float a = __uint_as_float(sreg[4 * i4]), b = __uint_as_float(sreg[4 * i4 + 1]);
-                    float cc = __uint_as_float(sreg[4 * i4 + 2]), d = __uint_as_float(sreg[4 * i4 + 3]);
-                    mul2(a, b, gv.x, gv.y);
-                    mul2(cc, d, gv.z, gv.w);
-                    sreg[4 * i4] = __float_as_uint(a);
-                    sreg[4 * i4 + 1] = __float_as_uint(b);
-                    sreg[4 * i4 + 2] = __float_as_uint(cc);
-                    sreg[4 * i4 + 3] = __float_as_uint(d);
-                }
-                tmem_st32(tS, sreg);
-                tmem_st32(tS + 32, sreg + 32);
-            }
-            // (B) delta^T = U^T - (S^T W^T) for rows 8hf .. 8hf+7
-            w = mbar_wait(bar(BAR_D1), c & 1, lim);
-            if (w) {
-                tc_fence_after();
-                float dsum[8];
-                ld_partials(c & 1, 0, dsum);
-                const float* U = reinterpret_cast<const float*>(smem + kSmRecv + ks * kOutBytes + kU);
-                uint32_t pk[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int r0 = 8 * hf + 2 * r;
-                    pk[r] = pack_bf16(U[r0 * kURow + j] - dsum[2 * r], U[(r0 + 1) * kURow + j] - dsum[2 * r + 1]);
-                }
-                tmem_st4(tDA, pk);
             }
             tmem_wait_st();
             tc_fence_before();
-            if (named_bar_or(kNamedK2, 256, !w)) { ok = false; break; }
-            tc_fence_after();
-            // State update (N = 128) and Mq delta into the output half of partial 0.
-            if (hf == 0 && quad < 2) {
-                if (elect_one()) {
-                    if (quad == 0)
-                        mma_ts(tmem + kColS, tmem + kColDA, sdesc(ob + kB2, kLbo, kSboB2), idesc128, 1);
-                    else if (with_out)
-                        mma_ts(tmem + kColD1 + 128u * (c & 1) + 16, tmem + kColDA,
-                               sdesc(ob + kB3, kLbo, kSboB3), idesc16, 1);
-                    tc_commit(bar(BAR_SDONE));
+            // Arrive on an issuer barrier.  After a failure the waits that pace the chain
+            // are skipped, so the chain then waits at the barrier too and can never be a
+            // generation ahead of the issuers.
+            auto chain_arrive = [&](uint32_t id, uint32_t count) {
+                if (*k2fail) named_bar_sync(id, count);
+                else named_bar_arrive(id, count);
+            };
+            chain_arrive(kNamedEmit, kEmitCount);  // EMIT(-1)
+            // Sum of the two K-half partials of 8 accumulator columns (rows 8hf..8hf+7);
+            // `col` selects the W (0) or the output (16) half of each partial.
+            auto ld_partials = [&](int buf, uint32_t col, float (&v)[8]) {
+                uint32_t a[8], b[8];
+                const uint32_t base = tmem + lanes + kColD1 + kD1Buf * (uint32_t)buf + col + 8 * hf;
+                tmem_ld8(base, a);
+                tmem_ld8(base + 32, b);
+                tmem_wait_ld_regs<8>(a);
+                tmem_wait_ld_regs<8>(b);
+#pragma unroll
+                for (int r = 0; r < 8; ++r) v[r] = __uint_as_float(a[r]) + __uint_as_float(b[r]);
+            };
+            // Output rows 8hf.. of chunk cp: through an output tile (stored by warp 12), or
+            // with plain stores (the last chunk of the sequence, possibly ragged).
+            auto emit_out = [&](int cp, bool tile_ok) {
+                const int64_t t0p = bos + (int64_t)cp * kChunk;
+                const int Cp = (eos - t0p < kChunk) ? (int)(eos - t0p) : kChunk;
+                float o[8];
+                ld_partials(cp & 1, 16, o);
+                if (tile_ok) {
+                    __nv_bfloat16* tile =
+                        reinterpret_cast<__nv_bfloat16*>(smem + kSmOTile + (cp % kOTiles) * kOTileBytes);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) tile[(8 * hf + r) * kD + j] = __float2bfloat16_rn(p.scale * o[r]);
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int row = 8 * hf + r;
+                        if (row < Cp) p.out[((t0p + row) * H + h) * kD + j] = __float2bfloat16_rn(p.scale * o[r]);
+                    }
                 }
-                __syncwarp();
+            };
+            for (int c = 0; c < nchunks; ++c) {
+                const bool has_next = c + 1 < nchunks;
+                const int ks = c % kRecvStages;
+                // The SDONE and D1 waits pace the chain against the issuers and are taken
+                // even after a failure (the issuers then commit without MMAs).
+                bool w = !*k2fail && k1_full(c);                           // U_c, exp(gam_C(c))
+                if (c > 0 && !mbar_wait(bar(BAR_SDONE), (c - 1) & 1, lim)) w = false;  // S_c complete
+                uint32_t pk[32];  // bf16 copy of D_{c+1}, written once MMA1(c) has read D_c
+                if (w) {
+                    tc_fence_after();
+                    // D_{c+1} = Diag(exp gam_C(c)) S_c, in place: warp 11 then adds Kbar_c^T delta_c.
+                    tmem_ld32(tS, sreg);
+                    tmem_ld32(tS + 32, sreg + 32);
+                    tmem_wait_ld_regs<64>(sreg);
+                    const float4* gc4 = reinterpret_cast<const float4*>(smem + kSmRecv + ks * kOutBytes + kGC) + 16 * hf;
+#pragma unroll
+                    for (int i4 = 0; i4 < 16; ++i4) {
+                        const float4 gv = gc4[i4];
+                        float a = __uint_as_float(sreg[4 * i4]), b = __uint_as_float(sreg[4 * i4 + 1]);
+                        float cc = __uint_as_float(sreg[4 * i4 + 2]), d = __uint_as_float(sreg[4 * i4 + 3]);
+                        mul2(a, b, gv.x, gv.y);
+                        mul2(cc, d, gv.z, gv.w);
+                        sreg[4 * i4] = __float_as_uint(a);
+                        sreg[4 * i4 + 1] = __float_as_uint(b);
+                        sreg[4 * i4 + 2] = __float_as_uint(cc);
+                        sreg[4 * i4 + 3] = __float_as_uint(d);
+                    }
+                    tmem_st32(tS, sreg);
+                    tmem_st32(tS + 32, sreg + 32);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        pk[i] = pack_bf16(__uint_as_float(sreg[2 * i]), __uint_as_float(sreg[2 * i + 1]));
+                }
+                if (!mbar_wait(bar(BAR_D1), c & 1, lim)) w = false;
+                {
+                    if (w) {
+                        tc_fence_after();
+                        // MMA1(c) has read D_c and [P_{c-1} ; R_{c-1}]: overwrite / hand back.
+                        if (warp == 8 && lane == 0 && c > 0) mbar_arrive(bar(BAR_PR_FREE + (c - 1) % kPRSlots));
+                        if (has_next) tmem_st32(tSA, pk);
+                        // delta^T = U^T - (W D + P delta_prev)^T for rows 8hf .. 8hf+7
+                        float dsum[8];
+                        ld_partials(c & 1, 0, dsum);
+                        const float* U = reinterpret_cast<const float*>(smem + kSmRecv + ks * kOutBytes + kU);
+                        uint32_t pk4[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int r0 = 8 * hf + 2 * r;
+                            pk4[r] = pack_bf16(U[r0 * kURow + j] - dsum[2 * r], U[(r0 + 1) * kURow + j] - dsum[2 * r + 1]);
+                        }
+                        tmem_st4(tmem + lanes + kColDA + 8u * (c & 1) + 4u * hf, pk4);
+                    }
+                }
+                if (!w) *k2fail = 1;
+                tmem_wait_st();
+                tc_fence_before();
+                chain_arrive(kNamedIssue, kIssueCount);  // ISSUE(c)
+                // Output of chunk c-1 (its Mq delta term completed with S_c), while the
+                // state update runs; the last chunk's output follows the loop.
+                if (w && c > 0 && with_out) emit_out(c - 1, true);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                chain_arrive(kNamedEmit, kEmitCount);  // EMIT(c)
             }
-            // (C) output rows of the previous chunk, while the state update runs
-            if (c > 0 && with_out && emit_out(c - 1)) tile_pending = c - 1;
-        }
-        if (ok && nchunks > 0) {
             // Output of the last chunk and the final state.
-            const bool w = mbar_wait(bar(BAR_SDONE), (nchunks - 1) & 1, lim);
-            if (store_issuer && lane == 0) bulk_wait_read0();
-            if (named_bar_or(kNamedK2, 256, !w)) {
-                ok = false;
-            } else {
+            const bool fin = !*k2fail && nchunks > 0 && mbar_wait(bar(BAR_SDONE), (nchunks - 1) & 1, lim);
+            if (fin) {
                 tc_fence_after();
-                issue_tile_store();
-                if (with_out && emit_out(nchunks - 1)) tile_pending = nchunks - 1;
-                named_bar_sync(kNamedK2, 256);
-                issue_tile_store();
+                if (with_out) emit_out(nchunks - 1, false);
             }
-        }
-        if (!ok) {
-            if (lane == 0) record(p.status, kStatusTimeout);
+            if (!*k2fail && write_final) {
+                tc_fence_after();
+                tmem_ld32(tS, sreg);
+                tmem_ld32(tS + 32, sreg + 32);
+                tmem_wait_ld_regs<64>(sreg);
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    p.sfin[foff + (size_t)(64 * hf + i) * kD + j] = __uint_as_float(sreg[i]);
+            } else if (nchunks > 0 && !fin) {
+                *k2fail = 1;
+            }
             tmem_wait_st();
             tmem_wait_ld();
-        } else if (write_final) {
-            tmem_ld32(tS, sreg);
-            tmem_ld32(tS + 32, sreg + 32);
-            tmem_wait_ld_regs<64>(sreg);
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-                p.sfin[foff + (size_t)(64 * hf + i) * kD + j] = __uint_as_float(sreg[i]);
         }
-        if (store_issuer && lane == 0) bulk_wait0();  // TMA stores complete before exit
-        // Drain every MMA this warp issued before TMEM is released.
-        if (elect_one()) tc_commit(bar(BAR_DRAIN));
-        __syncwarp();
-        if (!mbar_wait(bar(BAR_DRAIN), 0, kDrainLimit) && lane == 0) record(p.status, kStatusTimeout);
+        // Every MMA the three issuers started completes before TMEM is released.
+        if (warp == 0 || warp == 11 || warp == 12) {
+            if (elect_one()) tc_commit(bar(BAR_DRAIN));
+            __syncwarp();
+            if (!mbar_wait(bar(BAR_DRAIN), 0, kDrainLimit) && lane == 0) record(p.status, kStatusTimeout);
+        }
+        if (*k2fail && lane == 0) record(p.status, kStatusTimeout);
     }
 
     tc_fence_before();
