@@ -118,7 +118,9 @@ constexpr int kNumBars = 24;
 constexpr int kSmTmemSlot = kSmBar + kNumBars * 8;
 constexpr int kSmFail = kSmTmemSlot + 8;            // int32 per K1 group: failure flags
 constexpr int kSmK2Fail = kSmFail + 4 * kK1Groups;  // int32: K2 CTA failure flag
-constexpr int kSmemBytes = kSmK2Fail + 4;
+constexpr int kSmLanded = kSmK2Fail + 4;            // int32: K2 CTA, chunks landed so far
+constexpr int kSmPrReady = kSmLanded + 4;           // int32: K2 CTA, [P ; R] operands written
+constexpr int kSmemBytes = kSmPrReady + 4;
 static_assert(kSmPR + kPRSlots * kPRBytes <= kSmBar, "K2 buffers overlap the barriers");
 static_assert(kSmOTile % 128 == 0, "TMA store source must be 128-byte aligned");
 enum {  // K1 CTA barriers
@@ -217,6 +219,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(bar(BAR_SDONE), 1);
             mbar_init(bar(BAR_DRAIN), 3);
             *reinterpret_cast<volatile int32_t*>(smem + kSmK2Fail) = 0;
+            *reinterpret_cast<volatile int32_t*>(smem + kSmLanded) = 0;
+            *reinterpret_cast<volatile int32_t*>(smem + kSmPrReady) = 0;
             mbar_init(bar(BAR_NEVER), 1);
             for (int s = 0; s < kPRSlots; ++s) {
                 mbar_init(bar(BAR_PR_FULL + s), 1);
@@ -541,6 +545,12 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             return mbar_wait(bar(BAR_K1_FULL + c % kRecvStages), (c / kRecvStages) & 1, lim);
         };
         auto stage = [&](int c) { return sbase + kSmRecv + (uint32_t)(c % kRecvStages) * kOutBytes; };
+        // Progress counters published with release stores (relay: chunks landed; PR warp:
+        // lookahead operands written); a reader that sees enough progress skips the barrier
+        // wait, and otherwise falls back to it.
+        int32_t* landed = reinterpret_cast<int32_t*>(smem + kSmLanded);
+        int32_t* pr_ready = reinterpret_cast<int32_t*>(smem + kSmPrReady);
+        auto landed_or_wait = [&](int c) { return ld_acquire_cta(landed) > c || k1_full(c); };
         if ((p.debug_flags & 1) && !mbar_wait(bar(BAR_NEVER), 0, lim)) *k2fail = 1;  // never signalled
 
         if (warp == 9) {
@@ -549,8 +559,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (int c = 0; c < nchunks; ++c) {
                     if (!k1_full(c)) {
                         record(p.status, kStatusTimeout);
+                        *k2fail = 1;
                         break;
                     }
+                    st_release_cta(landed, c + 1);
                     mbar_arrive_remote_relaxed(mapa(bar(BAR_COPIED + c % kK1Groups), 0));
                 }
             }
@@ -611,10 +623,13 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             fence_proxy_async_smem();
             __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BAR_PR_FULL + slot));
+                if (lane == 0) {
+                    mbar_arrive(bar(BAR_PR_FULL + slot));
+                    st_release_cta(pr_ready, m + 1);
+                }
             }
         } else if (warp == 11) {
-            // ---- state update and Mq delta
+            // ---- state update S += Kbar_c^T delta_c
             // Every iteration commits, with or without MMAs: after a failure the commits
             // still pace the chain one generation at a time.
             for (int c = 0; c < nchunks; ++c) {
@@ -622,13 +637,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const bool live = !*k2fail;
                 tc_fence_after();
                 if (elect_one()) {
-                    if (live) {
-                        const uint32_t da = tmem + kColDA + 8u * (c & 1);
-                        mma_ts(tmem + kColS, da, sdesc(stage(c) + kB2, kLbo, kSboB2), idesc128, 1);
-                        if (with_out)
-                            mma_ts(tmem + kColD1 + kD1Buf * (c & 1) + 16, da, sdesc(stage(c) + kB3, kLbo, kSboB3),
-                                   idesc16, 1);
-                    }
+                    if (live)
+                        mma_ts(tmem + kColS, tmem + kColDA + 8u * (c & 1), sdesc(stage(c) + kB2, kLbo, kSboB2),
+                               idesc128, 1);
                     tc_commit(bar(BAR_SDONE));
                 }
                 __syncwarp();
@@ -638,7 +649,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     mbar_arrive_remote_relaxed(mapa(bar(BAR_OUT_FREE + (c - 1) % kRecvStages), 0));
             }
         } else if (warp == 12 || warp == 0) {
-            // ---- MMA1 over K half `kh` (warp 12: keys 0-63 plus the lookahead term)
+            // ---- after EMIT(c): warp 12 issues Mq_c delta_c (output of chunk c) and MMA1(c+1)
+            // over keys 0-63 plus the lookahead term; warp 0 issues MMA1(c+1) over keys
+            // 64-127 and then the output tile's TMA store.  Each commits to BAR_D1 once per
+            // EMIT generation (phase c+1), with or without MMAs (see warp 11).
             const int kh = warp == 12 ? 0 : 1;
             auto mma1 = [&](int c) {
                 const uint32_t d = tmem + kColD1 + kD1Buf * (c & 1) + 32u * kh;
@@ -651,50 +665,55 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (kh == 0 && c > 0)
                     mma_ts(d, tmem + kColDA + 8u * ((c - 1) & 1),
                            sdesc(sbase + kSmPR + ((c - 1) % kPRSlots) * kPRBytes, kLbo, kSboB3), idesc1, 1);
-                tc_commit(bar(BAR_D1));
             };
             // EMIT(-1): S_0 and its bf16 copy written
-            // Every chunk's MMA1 commit happens, with or without MMAs (see warp 11).
             named_bar_sync(kNamedEmit, kEmitCount);
             if (nchunks > 0) {
-                const bool live = !*k2fail && __all_sync(0xffffffffu, k1_full(0));
+                const bool live = !*k2fail && __all_sync(0xffffffffu, landed_or_wait(0));
                 if (!live && lane == 0) *k2fail = 1;
                 tc_fence_after();
                 if (elect_one()) {
                     if (live) mma1(0);
-                    else tc_commit(bar(BAR_D1));
+                    tc_commit(bar(BAR_D1));
                 }
                 __syncwarp();
             }
             for (int c = 0; c < nchunks; ++c) {
+                const bool has_next = c + 1 < nchunks;
+                // Operands of MMA1(c+1) are checked before the barrier: they do not
+                // depend on it, and the MMAs then go out right after it.
+                bool pre = true;
+                if (has_next && !*k2fail) {
+                    pre = landed_or_wait(c + 1);
+                    if (kh == 0)
+                        pre = pre && (ld_acquire_cta(pr_ready) > c ||
+                                      mbar_wait(bar(BAR_PR_FULL + c % kPRSlots), (c / kPRSlots) & 1, lim));
+                }
                 named_bar_sync(kNamedEmit, kEmitCount);  // EMIT(c)
-                bool live = !*k2fail;
+                bool live = !*k2fail && __all_sync(0xffffffffu, pre);
+                if (!live && lane == 0) *k2fail = 1;
                 tc_fence_after();
-                if (live && kh == 0 && c > 0 && with_out && lane == 0) {
-                    // output tile of chunk c-1 (written by the chain before EMIT(c)); the
-                    // chain refills a tile only after MMA1(c+1), so after this wait the
-                    // store of chunk c-4 (same tile as chunk c) has read its source
+                if (elect_one()) {
+                    if (live && kh == 0 && with_out)
+                        mma_ts(tmem + kColD1 + kD1Buf * (c & 1) + 16, tmem + kColDA + 8u * (c & 1),
+                               sdesc(stage(c) + kB3, kLbo, kSboB3), idesc16, 1);
+                    if (live && has_next) mma1(c + 1);
+                    tc_commit(bar(BAR_D1));
+                }
+                __syncwarp();
+                if (live && kh == 1 && c > 0 && with_out && lane == 0) {
+                    // Output tile of chunk c-1 (written by the chain before EMIT(c)).  The
+                    // chain refills this warp's tiles only after D1 phases this warp
+                    // commits later, so the drain below (all but the two newest stores)
+                    // covers the store of the chunk four back, whose tile comes next.
                     const int32_t t0p = (int32_t)(bos + (int64_t)(c - 1) * kChunk);
                     tma_store_3d(&tm_out, sbase + kSmOTile + ((c - 1) % kOTiles) * kOTileBytes, 0, h, t0p);
                     bulk_commit();
                     bulk_wait_read<2>();
                 }
                 __syncwarp();
-                if (c + 1 < nchunks) {
-                    if (live) {
-                        bool v = k1_full(c + 1);
-                        if (kh == 0) v = v && mbar_wait(bar(BAR_PR_FULL + c % kPRSlots), (c / kPRSlots) & 1, lim);
-                        live = __all_sync(0xffffffffu, v);
-                        if (!live && lane == 0) *k2fail = 1;
-                    }
-                    if (elect_one()) {
-                        if (live) mma1(c + 1);
-                        else tc_commit(bar(BAR_D1));
-                    }
-                    __syncwarp();
-                }
             }
-            if (kh == 0 && lane == 0) bulk_wait0();  // TMA stores complete before exit
+            if (kh == 1 && lane == 0) bulk_wait0();  // TMA stores complete before exit
         } else {
             // ---- state chain (warps 1-8, 256 threads)
             const int quad = warp & 3;                 // TMEM lane quadrant = SM sub-partition
@@ -779,7 +798,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const int ks = c % kRecvStages;
                 // The SDONE and D1 waits pace the chain against the issuers and are taken
                 // even after a failure (the issuers then commit without MMAs).
-                bool w = !*k2fail && k1_full(c);                           // U_c, exp(gam_C(c))
+                bool w = !*k2fail && landed_or_wait(c);                    // U_c, exp(gam_C(c))
                 if (c > 0 && !mbar_wait(bar(BAR_SDONE), (c - 1) & 1, lim)) w = false;  // S_c complete
                 uint32_t pk[32];  // bf16 copy of D_{c+1}, written once MMA1(c) has read D_c
                 if (w) {
@@ -831,15 +850,17 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_wait_st();
                 tc_fence_before();
                 chain_arrive(kNamedIssue, kIssueCount);  // ISSUE(c)
-                // Output of chunk c-1 (its Mq delta term completed with S_c), while the
+                // Output of chunk c-1 (its Mq delta term completed with D1(c)), while the
                 // state update runs; the last chunk's output follows the loop.
                 if (w && c > 0 && with_out) emit_out(c - 1, true);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 chain_arrive(kNamedEmit, kEmitCount);  // EMIT(c)
             }
-            // Output of the last chunk and the final state.
-            const bool fin = !*k2fail && nchunks > 0 && mbar_wait(bar(BAR_SDONE), (nchunks - 1) & 1, lim);
+            // Output of the last chunk (its Mq delta term commits to D1 phase nchunks) and
+            // the final state.
+            const bool fin = !*k2fail && nchunks > 0 && mbar_wait(bar(BAR_SDONE), (nchunks - 1) & 1, lim) &&
+                             mbar_wait(bar(BAR_D1), nchunks & 1, lim);
             if (fin) {
                 tc_fence_after();
                 if (with_out) emit_out(nchunks - 1, false);
