@@ -305,16 +305,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const bool with_out = (p.flags & kFlagNoOutput) == 0;
         for (int c = gi; c < nchunks; c += kK1Groups) {
             const int s = c % kInStages;
-            // One thread waits for the input tiles and for the landing of the group's
-            // previous bulk copy (its local operand buffer is rewritten below: a copy into
-            // the peer CTA completes only through the peer's barrier, which the K2 CTA
-            // relays back); the group barrier then publishes both to the group.
+            // One thread waits for the input tiles; the group barrier publishes them.
             bool ok = !fail_flag[gi];
-            if (kt == 0) {
-                ok = ok && mbar_wait(bar(BAR_IN_FULL + s), (c / kInStages) & 1, lim);
-                if (c >= kK1Groups)
-                    ok = ok && mbar_wait(bar(BAR_COPIED + gi), ((c / kK1Groups) - 1) & 1, lim);
-            }
+            if (kt == 0) ok = ok && mbar_wait(bar(BAR_IN_FULL + s), (c / kInStages) & 1, lim);
             if (named_bar_or(nbar, 128, !ok)) {
                 if (kt == 0) record(p.status, kStatusTimeout);
                 break;
@@ -341,12 +334,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float2 nrefl = make_float2(-refl.x, -refl.y);
             const float2 lastl = mul2f(gl[kChunk - 1], l2e2);
             const float2 ecr = ex2x2(add2(lastl, nrefl));     // exp(gam_C - gam_ref)
-            if (hr == 0) {
-                const float2 er = ex2x2(refl);
-                const float2 gc = ex2x2(lastl);
-                reinterpret_cast<float2*>(eref_sm)[pc] = er;
-                reinterpret_cast<float2*>(ob + kGC)[pc] = gc;
-            }
+            const float2 gcl = ex2x2(lastl);  // exp(gam_C), written to the operand buffer below
+            if (hr == 0) reinterpret_cast<float2*>(eref_sm)[pc] = ex2x2(refl);
             const uint32_t* q2 = reinterpret_cast<const uint32_t*>(in + kInQ);
             const uint32_t* k2 = reinterpret_cast<const uint32_t*>(in + kInK);
             const uint32_t* v2 = reinterpret_cast<const uint32_t*>(in + kInV);
@@ -378,16 +367,27 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     kb1[rr >> 1] = w >> 16;
                 }
             }
-            {   // Kbar rows 2pc, 2pc+1 of B2 (N = key channel, K = chunk row)
+            // The local operand buffer is written from here on: the group's previous bulk
+            // copy out of it must have landed (a copy into the peer CTA completes only
+            // through the peer's barrier, which the K2 CTA relays back).  Waiting this late
+            // gives that copy the whole of phase 1 to land.
+            bool copied = true;
+            if (kt == 0 && c >= kK1Groups)
+                copied = mbar_wait(bar(BAR_COPIED + gi), ((c / kK1Groups) - 1) & 1, lim);
+            if (named_bar_or(nbar, 128, !copied)) {
+                if (kt == 0) record(p.status, kStatusTimeout);
+                break;
+            }
+            if (kt == 0) mbar_arrive(bar(BAR_IN_EMPTY + s));  // input tiles consumed
+            {   // Kbar rows 2pc, 2pc+1 of B2 (N = key channel, K = chunk row), exp(gam_C)
                 unsigned char* b2 = ob + kB2;
                 const int c0 = 2 * pc, c1 = 2 * pc + 1;
                 *reinterpret_cast<uint4*>(b2 + (c0 >> 3) * kSboB2 + hr * kLbo + (c0 & 7) * 16) =
                     make_uint4(kb0[0], kb0[1], kb0[2], kb0[3]);
                 *reinterpret_cast<uint4*>(b2 + (c1 >> 3) * kSboB2 + hr * kLbo + (c1 & 7) * 16) =
                     make_uint4(kb1[0], kb1[1], kb1[2], kb1[3]);
+                if (hr == 0) reinterpret_cast<float2*>(ob + kGC)[pc] = gcl;
             }
-            named_bar_sync(nbar, 128);
-            if (kt == 0) mbar_arrive(bar(BAR_IN_EMPTY + s));  // input tiles consumed
 
             // Phase 2: warp 0 Gram A and the WY solve; warp 1 Gram Mq; warps 2-3 write
             // Qtil = (Q o exp(gam - gam_ref)) exp(gam_ref) into rows 16..31 of B1.
