@@ -21,28 +21,28 @@
 //
 // Mapping (transposed so the 128-wide value dim is the MMA's M):
 //   TMEM holds S^T (lane j = value column, column i = key row) in fp32.
-//   MMA1: P_W = S^T W^T and P_Q = S^T Qtil^T (A = bf16 copy of S^T in TMEM,
-//         B = [W ; Qtil] in shared memory), each as 4 K-quarter partial sums
-//   delta^T = U^T - sum(P_W)   (K2 threads, written back to TMEM as bf16)
-//   MMA2: S^T += delta^T . Kbar   (after the K2 threads scaled S^T by exp(gam_C))
-//   MMA3: P_Q += delta^T . Mq^T;  O^T = scale * sum(P_Q)
+//   One-chunk lookahead: with D_c = Diag(exp gam_C(c-1)) S_{c-1},
+//     W_c S_c = W_c D_c + P_{c-1} delta_{c-1},  P_{c-1} = W_c Kbar_{c-1}^T (Qtil, R alike),
+//   so MMA1 of chunk c (A = bf16 D_c^T in TMEM, B = [W ; Qtil]) needs only D_c.  Its
+//   accumulator also collects delta_{c-1}^T [P ; R]^T and V^T (-Tb)^T, hence
+//     delta_c^T = -(sum of the W partials),  O_c = scale (sum of the Qtil partials + Mq delta).
+//   MMA2: S^T += delta^T . Kbar, after the chain scaled S^T by exp(gam_C) in place.
 //
 // Work split (416 threads per CTA, 13 warps):
-//   CTA rank 0 ("K1 CTA"): warp 0 is the TMA producer (q/k/v/g tiles into a 4-stage
-//     ring; beta with plain loads, prefetched two chunks ahead); warps 1-12 are three
-//     K1 groups of 4 warps taking every third chunk (cumulative decay, decayed operands,
-//     in-chunk Grams and the WY solve; the 16x16 products use mma.sync because
-//     tcgen05's smallest M is 64).  A group writes its chunk's operands (21.8 KB) into
-//     a local buffer and ships them to the K2 CTA with one cp.async.bulk
-//     shared::cta -> shared::cluster copy that completes the K2 CTA's barrier.
-//   CTA rank 1 ("K2 CTA"): warp 0 owns TMEM; warps 1-8 run the state chain: state
-//     conversion/decay, delta, output, and the tcgen05 MMAs themselves.  The tensor
-//     pipe runs the MMAs of one issuing thread one after another but overlaps those of
-//     different warps, so MMA1 is split over the 4 K-quarters into partial accumulators
-//     issued by 4 warps (N = 32: W and Qtil together), and the state update (N = 128)
-//     and Mq delta are issued by two more.  Output rows of full chunks are staged in
-//     shared memory and written by one TMA tensor store per chunk.  K2 hands its
-//     3-stage receive ring back to K1 with remote mbarrier arrivals.
+//   CTA rank 0 ("K1 CTA"): warp 0 is the TMA producer (q/k/v/g tiles into a 6-stage
+//     ring; beta with plain loads, four chunks ahead); warps 1-12 are three K1 groups of
+//     4 warps taking every third chunk (cumulative decay, decayed operands, in-chunk
+//     Grams and the WY solve, W; the 16x16 products use mma.sync because tcgen05's
+//     smallest M is 64).  A group writes its chunk's operands (17.9 KB) into a local
+//     buffer and ships them to the K2 CTA with one cp.async.bulk shared::cta ->
+//     shared::cluster copy that completes the K2 CTA's barrier.
+//   CTA rank 1 ("K2 CTA"): warps 1-8 run the state chain (decay and bf16 copy of the
+//     state, delta, output rows) and only arrive on two named barriers; warp 11 issues
+//     the state update, warps 12 and 0 the Mq term and MMA1 of the next chunk (the
+//     tensor pipe runs one thread's MMAs in order but overlaps different threads'), warp
+//     0 also owns TMEM and issues the output tiles' TMA stores; warp 10 computes
+//     [P ; R] ahead of the chain; warp 9 relays copy landings back to the K1 groups and
+//     publishes how many chunks have landed.
 // Splitting a chain over two SMs doubles the shared-memory bandwidth and issue slots
 // each chunk gets; one SM alone was bound by its shared-memory pipe.
 // Every wait is bounded: on exhaustion the kernel records KDA_ERR_DEVICE_TIMEOUT in the
