@@ -46,10 +46,12 @@ _FWD_SOURCES = ["chunked_kda_delta_gb300/csrc/kda_fwd_tc.cu",
                 "chunked_kda_delta_gb300/csrc/kda_ptx.cuh",
                 "chunked_kda_delta_gb300/csrc/kda_internal.cuh"]
 KERNEL_SOURCES = {"serial": _FWD_SOURCES,
-                  "segment": _FWD_SOURCES + ["chunked_kda_delta_gb300/csrc/kda_merge.cu"]}
+                  "segment": _FWD_SOURCES + ["chunked_kda_delta_gb300/csrc/kda_merge.cu"],
+                  "auto": _FWD_SOURCES + ["chunked_kda_delta_gb300/csrc/kda_merge.cu"]}
 KERNEL_NAMES = {"serial": "kda_fwd_tc_kernel",
-                "segment": "kda_fwd_tc_kernel x3 + kda_merge_kernel (whole step)"}
-LAUNCHES_PER_STEP = {"serial": 1, "segment": 4}
+                "segment": "kda_fwd_tc_kernel x3 + kda_merge_kernel (whole step)",
+                "auto": "the plan the library picks (whole step)"}
+LAUNCHES_PER_STEP = {"serial": 1, "segment": 4, "auto": 1}
 
 
 def parse_args():
@@ -59,7 +61,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="single_t8192_h64")
-    ap.add_argument("--mode", choices=["serial", "segment"], default="serial")
+    ap.add_argument("--mode", choices=["serial", "segment", "auto"], default="serial")
     ap.add_argument("--segment-len", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
@@ -303,7 +305,10 @@ def workload_config(w, args, note=None):
                                             f"{w.num_seqs} sequences, {w.total_tokens} tokens"),
            "num_heads": w.num_heads, "head_dim": 128, "chunk": 16,
            "initial_state": w.has_initial_state, "final_state": True, "mode": args.mode,
-           "segment_len": (args.segment_len or 8192) if args.mode == "segment" else None,
+           "segment_len": ((args.segment_len or 8192) if args.mode == "segment" else
+                           (getattr(args, "planned", ("serial", 0))[1] or None) if args.mode == "auto"
+                           else None),
+           "plan": getattr(args, "planned", [args.mode])[0],
            "precision": "bf16 tensor-core operands, fp32 accumulation, fp32 state",
            "head_tokens_per_gpu": w.head_tokens, "parallelism": f"replicas x{args.gpus}",
            "l2": "no flush; inputs larger than L2 "
@@ -334,7 +339,15 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
-    mode = K.MODE_SEGMENT if args.mode == "segment" else K.MODE_SERIAL
+    mode = {"serial": K.MODE_SERIAL, "segment": K.MODE_SEGMENT, "auto": K.MODE_AUTO}[args.mode]
+    if args.mode == "auto":
+        # what the library will pick (its resident-cluster count is the occupancy query;
+        # one cluster per SM pair is the same on this part)
+        props = torch.cuda.get_device_properties(dev)
+        pm, ps = K.kda_plan(w.num_seqs if w.dense else 1, w.seq_lens[0] if w.dense else w.total_tokens,
+                            w.num_heads, max(1, props.multi_processor_count // 2),
+                            varlen=not w.dense, num_seqs=0 if w.dense else w.num_seqs)
+        args.planned = ("segment", ps) if pm == K.MODE_SEGMENT else ("serial", 0)
     inp, a, cu = device_inputs(K, w, dev)
     N = w.num_seqs
     out = torch.empty_like(a["q"])
@@ -352,7 +365,9 @@ def main():
     torch.cuda.synchronize()
     if K.kda_get_device_status() != 0:
         raise RuntimeError("device status error after warm-up")
-    launches_per_step = LAUNCHES_PER_STEP[args.mode]
+    launches_per_step = LAUNCHES_PER_STEP.get(args.mode, 1)
+    if args.mode == "auto":
+        launches_per_step = 4 if args.planned[0] == "segment" else 1
     if args.mode == "segment":
         seg = args.segment_len or 8192
         if w.dense and w.seq_lens[0] <= seg:

@@ -13,6 +13,7 @@ from .kda import (  # noqa: F401
     kda_get_device_status,
     kda_release_workspaces,
     kda_workspace_bytes,
+    kda_plan,
     load_library,
     MODE_SERIAL,
     MODE_SEGMENT,

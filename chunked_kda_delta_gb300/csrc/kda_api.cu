@@ -45,6 +45,7 @@ constexpr size_t kMaxWorkspaces = 8;
 struct DeviceInfo {
     bool ready = false;
     int cc_major = 0, cc_minor = 0, sm_count = 0;
+    int resident_clusters = 0;  // co-resident 2-CTA clusters of the fused kernel
     int32_t* status = nullptr;
 };
 
@@ -75,6 +76,26 @@ kda_status device_info(int dev, DeviceInfo** out) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kda::merge_smem_bytes())))
             return cuda_fail(e, "cudaFuncSetAttribute(merge kernel)");
+        {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2, 1, 1);
+            cfg.blockDim = dim3(kda::serial_block_threads(), 1, 1);
+            cfg.dynamicSmemBytes = kda::serial_smem_bytes();
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kda::serial_kernel_symbol(), &cfg) != cudaSuccess ||
+                n < 1) {
+                cudaGetLastError();  // clear; fall back to one cluster per SM pair
+                n = d.sm_count / 2;
+            }
+            d.resident_clusters = n > 0 ? n : 1;
+        }
         d.ready = true;
     }
     *out = &d;
@@ -323,6 +344,48 @@ struct SegPlan {
     size_t off_b = 0, off_m = 0, off_c = 0, bytes = 0;
 };
 
+// Serial or segment mode, and the segment length, for a problem with `resident`
+// co-resident clusters.  Cost unit: one chunk period of one state chain.  Every pass of
+// the fused kernel (serial; segment summary, transition and output passes) costs about
+// the same per chunk on GB300 (T = 131072, H = 64: serial 0.925 us per chunk, the segment
+// passes 0.908 us per chunk of the busiest cluster slot), clusters beyond `resident` run
+// in further waves, and each segment adds a fixed cost (the merge walks a chain's
+// segments one after another; each short cluster fills its pipeline).  Fitted on GB300
+// from T = 131072, H = 4 with segments of 512 .. 8192 tokens (1.55 .. 4.99 ms against
+// 7.53 ms serial): about 15 chunk periods per segment, within 5% at every point.
+constexpr double kMergePerSegment = 15.0;
+constexpr double kSegmentMargin = 0.8;      // segment mode must win by 20%
+constexpr size_t kPlanWorkspaceCap = (size_t)4 << 30;
+
+void choose_plan(const Problem& pr, int64_t resident, int32_t* mode, int32_t* seg_len) {
+    *mode = KDA_MODE_SERIAL;
+    *seg_len = 0;
+    if (pr.varlen || pr.dense_len <= 0) return;
+    const int64_t C = (int64_t)pr.N * pr.H;
+    const int64_t R = resident > 0 ? resident : 1;
+    auto cdiv = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
+    const int64_t nck = cdiv(pr.dense_len, kda::kChunk);
+    const double serial = (double)cdiv(C, R) * (double)nck;
+    double best = serial;
+    int32_t best_len = 0;
+    for (int64_t sl = 512; sl <= ((int64_t)1 << 20); sl *= 2) {
+        const int64_t nseg = cdiv(pr.dense_len, sl);
+        if (nseg < 2) break;
+        const size_t ws = (size_t)(3 * nseg - 2) * (size_t)C * kda::kD * kda::kD * 4;
+        if (ws > kPlanWorkspaceCap) continue;
+        const double waves = (double)(2 * cdiv(C * (nseg - 1), R) + cdiv(C * nseg, R));
+        const double cost = waves * (double)(sl / kda::kChunk) + kMergePerSegment * (double)nseg;
+        if (cost < best) {
+            best = cost;
+            best_len = (int32_t)sl;
+        }
+    }
+    if (best_len && best < kSegmentMargin * serial) {
+        *mode = KDA_MODE_SEGMENT;
+        *seg_len = best_len;
+    }
+}
+
 SegPlan plan_segments(const Problem& pr, int32_t seg_len) {
     SegPlan sp;
     if (pr.varlen || pr.dense_len <= 0 || seg_len <= 0) return sp;
@@ -377,6 +440,7 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
             (st = encode_chunk_map(&maps.out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "out")))
             return st;
     }
+    if (mode == KDA_MODE_AUTO) choose_plan(pr, di->resident_clusters, &mode, &seg_len);
     const SegPlan sp = mode == KDA_MODE_SEGMENT ? plan_segments(pr, seg_len) : SegPlan{};
     if (sp.nseg <= 1) {
         e = kda::launch_serial(p, maps, stream);
@@ -528,7 +592,27 @@ kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, 
     int64_t wait_limit;
     if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit, &debug_flags)) != KDA_OK)
         return st;
+    if (mode == KDA_MODE_AUTO) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+        DeviceInfo* di = nullptr;
+        if ((st = device_info(dev, &di)) != KDA_OK) return st;
+        choose_plan(pr, di->resident_clusters, &mode, &seg_len);
+    }
     *bytes = mode == KDA_MODE_SEGMENT ? plan_segments(pr, seg_len).bytes : 0;
+    return KDA_OK;
+}
+
+kda_status kda_plan(const kda_shape* shape, int32_t varlen, int32_t resident_clusters, int32_t* mode,
+                    int32_t* segment_len) {
+    t_last_error[0] = '\0';
+    if (!mode || !segment_len) return fail(KDA_ERR_INVALID_ARGUMENT, "mode or segment_len is NULL");
+    if (resident_clusters < 1) return fail(KDA_ERR_INVALID_ARGUMENT, "resident_clusters must be >= 1");
+    Problem pr{};
+    kda_status st = validate_shape(shape, varlen != 0, &pr);
+    if (st != KDA_OK) return st;
+    choose_plan(pr, resident_clusters, mode, segment_len);
     return KDA_OK;
 }
 

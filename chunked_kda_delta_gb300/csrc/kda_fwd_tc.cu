@@ -899,6 +899,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 }  // namespace
 
 size_t serial_smem_bytes() { return kSmemBytes; }
+int serial_block_threads() { return kThreads; }
 const void* serial_kernel_symbol() { return reinterpret_cast<const void*>(&kda_fwd_tc_kernel); }
 
 cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream_t stream) {

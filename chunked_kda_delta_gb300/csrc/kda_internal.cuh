@@ -90,6 +90,7 @@ cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream
 cudaError_t launch_merge(const float* m_seg, const float* b_seg, const float* s0, float* carries,
                          int32_t B, int32_t nseg, int32_t H, cudaStream_t stream);
 size_t serial_smem_bytes();
+int serial_block_threads();
 const void* serial_kernel_symbol();
 size_t merge_smem_bytes();
 const void* merge_kernel_symbol();

@@ -69,6 +69,9 @@ WORKLOADS = {
     "batch4_t4096_h128": Workload("batch4_t4096_h128", (4096,) * 4, 128, True, True, 2),
     "varlen_h12": Workload("varlen_h12", varlen_h12_lengths(3), 12, False, False, 3),
     "long_t131072_h64": Workload("long_t131072_h64", (131072,), 64, False, True, 4),
+    # the long-sequence distributions with few heads: too few chains to fill the GPU
+    # serially, the case the segment planner exists for
+    "long_t131072_h4": Workload("long_t131072_h4", (131072,), 4, False, True, 5),
 }
 
 

@@ -29,7 +29,7 @@ _STATUS = {
 EXPORTED_SYMBOLS = (
     "kda_prefill", "kda_prefill_ex", "kda_prefill_host", "kda_workspace_bytes",
     "kda_get_device_status", "kda_release_workspaces", "kda_status_string",
-    "kda_last_error_message", "kda_version", "kda_prefill_segment_noalloc",
+    "kda_last_error_message", "kda_version", "kda_prefill_segment_noalloc", "kda_plan",
 )
 
 
@@ -83,6 +83,8 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False) -> 
             f32p, ctypes.c_int32, vp]
         lib.kda_workspace_bytes.argtypes = [ctypes.POINTER(KdaShape), ctypes.POINTER(KdaOptions),
                                             ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_plan.argtypes = [ctypes.POINTER(KdaShape), ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         lib.kda_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         lib.kda_release_workspaces.argtypes = [ctypes.c_int32]
         lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -91,7 +93,7 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False) -> 
         lib.kda_version.restype = ctypes.c_char_p
         for f in (lib.kda_prefill, lib.kda_prefill_ex, lib.kda_prefill_host,
                   lib.kda_prefill_segment_noalloc,
-                  lib.kda_workspace_bytes, lib.kda_get_device_status,
+                  lib.kda_workspace_bytes, lib.kda_get_device_status, lib.kda_plan,
                   lib.kda_release_workspaces):
             f.restype = ctypes.c_int
         if path is None:
@@ -253,6 +255,18 @@ def kda_workspace_bytes(batch: int, seq_len: int, num_heads: int, mode: int = MO
     _check(lib, lib.kda_workspace_bytes(ctypes.byref(shape), ctypes.byref(opts),
                                         ctypes.byref(n)))
     return int(n.value)
+
+
+def kda_plan(batch: int, seq_len: int, num_heads: int, resident_clusters: int,
+             varlen: bool = False, num_seqs: int = 0, head_dim: int = 128):
+    """The (mode, segment_len) that ``MODE_AUTO`` picks for this shape on a device holding
+    ``resident_clusters`` co-resident clusters.  Host only."""
+    lib = load_library()
+    shape = KdaShape(batch, seq_len, num_seqs, num_heads, head_dim)
+    mode, seg = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib, lib.kda_plan(ctypes.byref(shape), int(bool(varlen)), int(resident_clusters),
+                             ctypes.byref(mode), ctypes.byref(seg)))
+    return int(mode.value), int(seg.value)
 
 
 def kda_get_device_status(stream=None, device=None) -> int:

@@ -163,8 +163,22 @@ kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q
                                        float* final_state, int32_t segment_len, void* stream);
 
 /* Bytes of device workspace a call with this shape and these options uses
- * (0 for serial mode).  No device work; *bytes is written on success. */
+ * (0 for serial mode).  No device work, except that KDA_MODE_AUTO reads the current
+ * device's resident cluster count to resolve the plan; *bytes is written on success. */
 kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, size_t* bytes);
+
+/* The execution plan KDA_MODE_AUTO picks for this shape on a device that holds
+ * `resident_clusters` co-resident clusters of the fused kernel (kda_prefill_ex uses
+ * the current device's count): KDA_MODE_SERIAL (*segment_len = 0) or
+ * KDA_MODE_SEGMENT with *segment_len tokens per segment.  Packed varlen input
+ * (`varlen` != 0) is always serial.  The cost model counts chunk periods of one
+ * state chain: every pass of the fused kernel costs about the same per chunk,
+ * clusters beyond the resident count run in further waves, and the merge walks a
+ * chain's segments in order (segment-parallel prefill, cuLA PR #103 "intracard-CP
+ * prefill", planner notes).  Host only, no device work.  Errors:
+ * KDA_ERR_INVALID_ARGUMENT for a bad shape, NULL outputs or resident_clusters < 1. */
+kda_status kda_plan(const kda_shape* shape, int32_t varlen, int32_t resident_clusters, int32_t* mode,
+                    int32_t* segment_len);
 
 /* Reads and clears the device status word of the current device after
  * synchronising `stream`.  *code receives KDA_OK, KDA_ERR_INVALID_ARGUMENT

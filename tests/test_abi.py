@@ -136,3 +136,33 @@ def test_binding_checks_dtypes():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(K.KdaError):
         K.load_library(str(tmp_path / "nope.so"))
+
+
+def test_planner_decisions(lib):
+    """The AUTO plan (host only): segment mode only when the chains alone cannot fill the
+    GPU and the sequence is long; never for varlen input or a single chunk."""
+    R = 76
+    assert K.kda_plan(1, 131072, 64, R) == (K.MODE_SERIAL, 0)
+    assert K.kda_plan(4, 4096, 128, R) == (K.MODE_SERIAL, 0)
+    assert K.kda_plan(1, 64, 4, R) == (K.MODE_SERIAL, 0)
+    assert K.kda_plan(1, 131072, 4, R, varlen=True, num_seqs=3) == (K.MODE_SERIAL, 0)
+    m, s = K.kda_plan(1, 131072, 4, R)
+    assert m == K.MODE_SEGMENT and s > 0 and s % 16 == 0 and s < 131072
+    m, s = K.kda_plan(1, 32768, 2, R)
+    assert m == K.MODE_SEGMENT and s % 16 == 0
+
+
+@pytest.mark.parametrize("chains_per_cluster", [1, 2])
+@pytest.mark.parametrize("T", [16384, 131072, 1 << 20])
+def test_planner_keeps_serial_when_chains_fill_the_gpu(lib, chains_per_cluster, T):
+    # With at least one chain per resident cluster, every segment plan needs at least
+    # 3 nseg - 2 waves of segment passes against one or more serial waves: never a win.
+    R = 76
+    assert K.kda_plan(1, T, R * chains_per_cluster, R)[0] == K.MODE_SERIAL
+
+
+def test_planner_rejects_bad_arguments(lib):
+    with pytest.raises(K.KdaError):
+        K.kda_plan(1, 1000, 4, 0)
+    with pytest.raises(K.KdaError):
+        K.kda_plan(1, 1000, 4, 76, head_dim=64)

@@ -112,3 +112,26 @@ def test_capture_without_warmup_is_refused():
     g2.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+def test_auto_mode_plans_segments_for_few_chains(orc):
+    """Two chains on a GPU that holds dozens of clusters: MODE_AUTO takes the segment
+    path the planner reports, matches the oracle, and sizes its workspace the same way."""
+    T, H = 32768, 2
+    resident = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    m, seg = K.kda_plan(1, T, H, resident)
+    assert m == K.MODE_SEGMENT
+    assert K.kda_workspace_bytes(1, T, H, mode=K.MODE_AUTO) == \
+        K.kda_workspace_bytes(1, T, H, mode=K.MODE_SEGMENT, segment_len=seg)
+    inp = make_inputs(custom([T], H, True, seed=320), DEV)
+    out, fin = run(inp, K.MODE_AUTO)
+    o_ref, f_ref = oracle_on_heads(orc, inp, range(H))
+    assert_close(gpu_out_heads(out, range(H)), o_ref, "auto out")
+    assert_close(gpu_state_heads(fin, range(H)), f_ref, "auto final")
+    o_ser, f_ser = run(inp, K.MODE_SERIAL)
+    print(f"\nauto (segment_len {seg}) vs serial max |diff|: out "
+          f"{(out.float() - o_ser.float()).abs().max().item():.3e}")
+
+
+def test_auto_mode_keeps_serial_for_many_chains():
+    assert K.kda_workspace_bytes(1, 8192, 64, mode=K.MODE_AUTO) == 0
