@@ -93,10 +93,20 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_hash(mode: str) -> str:
+def _code_only(text: str) -> str:
+    """C/C++ source without comments, whitespace runs collapsed (the sources hold no
+    comment markers inside string literals): comment edits keep the hash."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", " ", text).strip()
+
+
+def source_hash(mode: str, read=None) -> str:
+    """Hash of the code (not the comments) of the kernel sources a mode runs."""
+    read = read or (lambda rel: open(os.path.join(ROOT, rel)).read())
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES.get(mode, []):
-        h.update(open(os.path.join(ROOT, rel), "rb").read())
+        h.update(_code_only(read(rel)).encode())
     return h.hexdigest()[:16]
 
 

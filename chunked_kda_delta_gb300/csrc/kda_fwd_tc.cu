@@ -24,16 +24,16 @@
 //   One-chunk lookahead: with D_c = Diag(exp gam_C(c-1)) S_{c-1},
 //     W_c S_c = W_c D_c + P_{c-1} delta_{c-1},  P_{c-1} = W_c Kbar_{c-1}^T (Qtil, R alike),
 //   so MMA1 of chunk c (A = bf16 D_c^T in TMEM, B = [W ; Qtil]) needs only D_c.  Its
-//   accumulator also collects delta_{c-1}^T [P ; R]^T and V^T (-Tb)^T, hence
-//     delta_c^T = -(sum of the W partials),  O_c = scale (sum of the Qtil partials + Mq delta).
+//   accumulator also collects delta_{c-1}^T [P ; R]^T, hence
+//     delta_c^T = U_c^T - (sum of the W partials),  O_c = scale (sum of the Qtil partials + Mq delta).
 //   MMA2: S^T += delta^T . Kbar, after the chain scaled S^T by exp(gam_C) in place.
 //
 // Work split (416 threads per CTA, 13 warps):
-//   CTA rank 0 ("K1 CTA"): warp 0 is the TMA producer (q/k/v/g tiles into a 6-stage
-//     ring; beta with plain loads, four chunks ahead); warps 1-12 are three K1 groups of
+//   CTA rank 0 ("K1 CTA"): warp 0 is the TMA producer (q/k/v/g tiles into a 4-stage
+//     ring; beta with plain loads, two chunks ahead); warps 1-12 are three K1 groups of
 //     4 warps taking every third chunk (cumulative decay, decayed operands, in-chunk
-//     Grams and the WY solve, W; the 16x16 products use mma.sync because tcgen05's
-//     smallest M is 64).  A group writes its chunk's operands (17.9 KB) into a local
+//     Grams and the WY solve, W and U; the 16x16 products use mma.sync because tcgen05's
+//     smallest M is 64).  A group writes its chunk's operands (21.8 KB) into a local
 //     buffer and ships them to the K2 CTA with one cp.async.bulk shared::cta ->
 //     shared::cluster copy that completes the K2 CTA's barrier.
 //   CTA rank 1 ("K2 CTA"): warps 1-8 run the state chain (decay and bf16 copy of the
