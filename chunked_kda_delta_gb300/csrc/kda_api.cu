@@ -281,8 +281,6 @@ kda_status validate_options(const kda_options* o, const Problem& pr, int32_t* mo
                     "segment_len must be a non-negative multiple of 16 (got %d)", o->segment_len);
     if (o->wait_limit < 0)
         return fail(KDA_ERR_INVALID_ARGUMENT, "wait_limit must be >= 0");
-    if (o->mode == KDA_MODE_SEGMENT && pr.varlen)
-        return fail(KDA_ERR_INVALID_ARGUMENT, "segment mode needs dense input (no cu_seqlens)");
     *mode = o->mode;
     if (o->segment_len) *seg_len = o->segment_len;
     if (o->wait_limit) *wait_limit = o->wait_limit;
@@ -386,6 +384,28 @@ void choose_plan(const Problem& pr, int64_t resident, int32_t* mode, int32_t* se
     }
 }
 
+// Varlen segment plan: sequence n gets max(1, ceil(len_n / seg_len)) segments, at most
+// N + floor(T_total / seg_len) in all; the table, summaries, transitions and carries are
+// sized for that bound (rows past the actual count exit at once).
+struct VarSegPlan {
+    int64_t rows = 0;  // 0: serial
+    size_t off_tab = 0, off_b = 0, off_m = 0, off_c = 0, bytes = 0;
+};
+
+VarSegPlan plan_segments_varlen(const Problem& pr, int32_t seg_len) {
+    VarSegPlan vp;
+    if (!pr.varlen || seg_len <= 0 || pr.T_total <= seg_len) return vp;
+    vp.rows = (int64_t)pr.N + pr.T_total / seg_len;
+    const size_t st = (size_t)kda::kD * kda::kD * 4;
+    const size_t per = (size_t)vp.rows * pr.H * st;
+    vp.off_tab = 0;
+    vp.off_b = ((size_t)(pr.N + 1) * 4 + 255) / 256 * 256;
+    vp.off_m = vp.off_b + per;
+    vp.off_c = vp.off_m + per;
+    vp.bytes = vp.off_c + per;
+    return vp;
+}
+
 SegPlan plan_segments(const Problem& pr, int32_t seg_len) {
     SegPlan sp;
     if (pr.varlen || pr.dense_len <= 0 || seg_len <= 0) return sp;
@@ -441,6 +461,50 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
             return st;
     }
     if (mode == KDA_MODE_AUTO) choose_plan(pr, di->resident_clusters, &mode, &seg_len);
+    if (mode == KDA_MODE_SEGMENT && pr.varlen) {
+        const VarSegPlan vp = plan_segments_varlen(pr, seg_len);
+        if (vp.rows > 0) {
+            if (vp.rows * 2 * pr.H > 0x7fffffffll)
+                return fail(KDA_ERR_INVALID_ARGUMENT, "too many segments for one launch");
+            // Varlen segments: table -> pre_scan (summaries from zero, transitions from the
+            // identity; every segment but each sequence's last) -> merge -> segment-K2.
+            void* ws = nullptr;
+            if ((st = get_workspace(dev, stream, kWsSegment, vp.bytes, &ws)) != KDA_OK) return st;
+            char* base = static_cast<char*>(ws);
+            int32_t* table = reinterpret_cast<int32_t*>(base + vp.off_tab);
+            float* b_seg = reinterpret_cast<float*>(base + vp.off_b);
+            float* m_seg = reinterpret_cast<float*>(base + vp.off_m);
+            float* carries = reinterpret_cast<float*>(base + vp.off_c);
+            if ((e = kda::launch_segment_table(cu, pr.N, pr.T_total, seg_len, table, di->status,
+                                               stream)) != cudaSuccess)
+                return cuda_fail(e, "segment table launch");
+            kda::FwdParams ps = p;
+            ps.seg_len = seg_len;
+            ps.seg_start = table;
+            ps.rows = (int32_t)vp.rows;
+            ps.s0 = nullptr;
+            ps.sfin = b_seg;
+            ps.flags = kda::kFlagNoOutput | kda::kFlagSkipLastSeg;
+            if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
+                return cuda_fail(e, "pre_scan (summary) launch");
+            ps.sfin = m_seg;
+            ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0 | kda::kFlagSkipLastSeg;
+            if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
+                return cuda_fail(e, "pre_scan (transition) launch");
+            if ((e = kda::launch_merge(m_seg, b_seg, s0, carries, pr.N, 0, pr.H, stream, table)) !=
+                cudaSuccess)
+                return cuda_fail(e, "merge launch");
+            kda::FwdParams pk = p;
+            pk.seg_len = seg_len;
+            pk.seg_start = table;
+            pk.rows = (int32_t)vp.rows;
+            pk.s0 = carries;
+            pk.flags = kda::kFlagFinalLastSeg;
+            if ((e = kda::launch_serial(pk, maps, stream)) != cudaSuccess)
+                return cuda_fail(e, "segment-K2 launch");
+            return KDA_OK;
+        }
+    }
     const SegPlan sp = mode == KDA_MODE_SEGMENT ? plan_segments(pr, seg_len) : SegPlan{};
     if (sp.nseg <= 1) {
         e = kda::launch_serial(p, maps, stream);
@@ -586,12 +650,16 @@ kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, 
     t_last_error[0] = '\0';
     if (!bytes) return fail(KDA_ERR_INVALID_ARGUMENT, "bytes is NULL");
     Problem pr{};
-    kda_status st = validate_shape(shape, false, &pr);
+    kda_status st = validate_shape(shape, shape && shape->num_seqs > 0, &pr);
     if (st != KDA_OK) return st;
     int32_t mode, seg_len, debug_flags;
     int64_t wait_limit;
     if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit, &debug_flags)) != KDA_OK)
         return st;
+    if (mode == KDA_MODE_SEGMENT && pr.varlen) {
+        *bytes = plan_segments_varlen(pr, seg_len).bytes;
+        return KDA_OK;
+    }
     if (mode == KDA_MODE_AUTO) {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);

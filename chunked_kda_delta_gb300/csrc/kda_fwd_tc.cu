@@ -194,7 +194,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int h = unit % p.H;
     const int n = unit / p.H;
     int64_t bos, eos;
-    if (!seq_range(p, n, bos, eos)) return;   // both CTAs of the cluster return
+    int seq_id, seg_id, seg_count;
+    if (!seq_range(p, n, bos, eos, seq_id, seg_id, seg_count)) return;  // both CTAs return
     const int64_t H = p.H;
     const int nchunks = (int)((eos - bos + kChunk - 1) / kChunk);
     const int64_t lim = p.wait_limit;
@@ -728,9 +729,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             size_t foff = soff;
             bool write_final = p.sfin != nullptr;
             if (p.flags & kFlagFinalLastSeg) {
-                const int b = n / p.nseg_used, sg = n % p.nseg_used;
-                write_final = write_final && sg == p.nseg_total - 1;
-                foff = ((size_t)b * p.H + h) * kD * kD;
+                write_final = write_final && seg_id == seg_count - 1;
+                foff = ((size_t)seq_id * p.H + h) * kD * kD;
             }
             uint32_t sreg[64];
             // Initial state S0[i][j] for keys i of this half -> S^T[j][i], and its bf16 copy.
@@ -903,7 +903,8 @@ int serial_block_threads() { return kThreads; }
 const void* serial_kernel_symbol() { return reinterpret_cast<const void*>(&kda_fwd_tc_kernel); }
 
 cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream_t stream) {
-    const long long rows = p.seg_len > 0 ? (long long)p.N * p.nseg_used : (long long)p.N;
+    const long long rows = p.seg_len > 0 ? (p.cu ? (long long)p.rows : (long long)p.N * p.nseg_used)
+                                         : (long long)p.N;
     const long long clusters = rows * p.H;
     if (clusters == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};

@@ -36,30 +36,61 @@ struct FwdParams {
     int64_t wait_limit;   // iteration limit of bounded spin waits
     int32_t debug_flags;  // KDA_DEBUG_* bits (failure-path tests only)
     int32_t* status;      // device status word of this device
-    // Segment launches (seg_len > 0): CTA row n' = b * nseg_used + s runs segment s of
-    // dense sequence b, tokens [b*L + s*seg_len, b*L + min((s+1)*seg_len, L)), L = dense_len.
+    // Segment launches (seg_len > 0).  Dense: CTA row n' = b * nseg_used + s runs segment s
+    // of sequence b, tokens [b*L + s*seg_len, b*L + min((s+1)*seg_len, L)), L = dense_len.
+    // Varlen (cu != nullptr): row n' is global segment n' of the table seg_start (sequence
+    // n owns rows seg_start[n] .. seg_start[n+1]-1, at least one), tokens
+    // [cu[n] + s*seg_len, min(cu[n] + (s+1)*seg_len, cu[n+1])); rows past seg_start[N]
+    // exit.
     int64_t seg_len;
-    int32_t nseg_used;    // segments of each sequence covered by this launch
-    int32_t nseg_total;   // segments of each sequence
+    int32_t nseg_used;    // dense: segments of each sequence covered by this launch
+    int32_t nseg_total;   // dense: segments of each sequence
     int32_t flags;        // kFlag* below
+    const int32_t* seg_start;  // varlen segment table [N + 1] (device), or nullptr
+    int32_t rows;         // varlen segment launches: rows launched (an upper bound)
 };
 
 // Launch flags of the fused kernel.
 constexpr int32_t kFlagNoOutput = 1;       // no output rows (summary runs)
 constexpr int32_t kFlagZeroV = 2;          // treat v as zero (transition runs: U = 0)
 constexpr int32_t kFlagIdentityS0 = 4;     // initial state = identity
-constexpr int32_t kFlagFinalLastSeg = 8;   // write final state only for the last segment, at index b
+constexpr int32_t kFlagFinalLastSeg = 8;   // write final state only for the last segment, at its sequence
+constexpr int32_t kFlagSkipLastSeg = 16;   // varlen summaries: the last segment of a sequence is not run
 
 // Token range [bos, eos) of sequence n; false (and the status word set) when
 // cu_seqlens is malformed for this sequence.
-__device__ __forceinline__ bool seq_range(const FwdParams& p, int n, int64_t& bos,
-                                          int64_t& eos) {
-    if (p.seg_len > 0) {
-        const int b = n / p.nseg_used, sg = n % p.nseg_used;
-        const int64_t base = (int64_t)b * p.dense_len;
+// Token range of CTA row n, with its sequence, segment index and the sequence's segment
+// count (1 and 0 outside segment launches).  False: nothing to run for this row.
+__device__ __forceinline__ bool seq_range(const FwdParams& p, int n, int64_t& bos, int64_t& eos,
+                                          int& seq, int& sg, int& nsg) {
+    seq = n;
+    sg = 0;
+    nsg = 1;
+    if (p.seg_len > 0 && p.cu == nullptr) {
+        seq = n / p.nseg_used;
+        sg = n % p.nseg_used;
+        nsg = p.nseg_total;
+        const int64_t base = (int64_t)seq * p.dense_len;
         const int64_t a = (int64_t)sg * p.seg_len;
         bos = base + a;
         eos = base + (a + p.seg_len < p.dense_len ? a + p.seg_len : p.dense_len);
+        return true;
+    }
+    if (p.seg_len > 0) {
+        if (n >= p.seg_start[p.N]) return false;
+        int lo = 0, hi = p.N - 1;  // last sequence whose first row is <= n
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.seg_start[mid] <= n) lo = mid;
+            else hi = mid - 1;
+        }
+        seq = lo;
+        sg = n - p.seg_start[lo];
+        nsg = p.seg_start[lo + 1] - p.seg_start[lo];
+        if ((p.flags & kFlagSkipLastSeg) && sg == nsg - 1) return false;
+        const int64_t end = p.cu[seq + 1];
+        bos = p.cu[seq] + (int64_t)sg * p.seg_len;
+        eos = bos + p.seg_len < end ? bos + p.seg_len : end;
         return true;
     }
     if (p.cu == nullptr) {
@@ -87,8 +118,15 @@ struct TensorMaps {
 // Fused K1+K2 kernel over p.N x p.H rows (or the segment rows of a segment launch).
 cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream_t stream);
 // Segment merge: carry[b][0] = S0[b] (or 0), carry[b][s+1] = m[b][s] carry[b][s] + bs[b][s].
+// Varlen segment table: seg_start[n] = sum over sequences before n of
+// max(1, ceil(len / seg_len)); validates cu_seqlens (status word on malformed input).
+cudaError_t launch_segment_table(const int32_t* cu, int32_t N, int64_t T_total, int64_t seg_len,
+                                 int32_t* seg_start, int32_t* status, cudaStream_t stream);
+// Dense: B sequences of nseg segments.  Varlen (seg_start != nullptr): B = N sequences,
+// each with its own count from the table; summaries and carries indexed by segment row.
 cudaError_t launch_merge(const float* m_seg, const float* b_seg, const float* s0, float* carries,
-                         int32_t B, int32_t nseg, int32_t H, cudaStream_t stream);
+                         int32_t B, int32_t nseg, int32_t H, cudaStream_t stream,
+                         const int32_t* seg_start = nullptr);
 size_t serial_smem_bytes();
 int serial_block_threads();
 const void* serial_kernel_symbol();

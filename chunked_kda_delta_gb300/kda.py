@@ -246,10 +246,11 @@ def kda_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
 
 
 def kda_workspace_bytes(batch: int, seq_len: int, num_heads: int, mode: int = MODE_SERIAL,
-                        segment_len: int = 0, head_dim: int = 128) -> int:
-    """Device workspace bytes for a dense problem of this shape in this mode."""
+                        segment_len: int = 0, head_dim: int = 128, num_seqs: int = 0) -> int:
+    """Device workspace bytes for a problem of this shape in this mode (packed varlen
+    when ``num_seqs`` > 0: ``batch`` 1, ``seq_len`` the total tokens)."""
     lib = load_library()
-    shape = KdaShape(batch, seq_len, 0, num_heads, head_dim)
+    shape = KdaShape(batch, seq_len, num_seqs, num_heads, head_dim)
     opts = _options(mode, segment_len, 0)
     n = ctypes.c_size_t(0)
     _check(lib, lib.kda_workspace_bytes(ctypes.byref(shape), ctypes.byref(opts),

@@ -81,7 +81,7 @@ typedef struct kda_shape {
 
 /* Execution modes of kda_prefill_ex. */
 #define KDA_MODE_SERIAL 0   /* one fused K1+K2 chain per (sequence, head) */
-#define KDA_MODE_SEGMENT 1  /* segment-parallel: K1 -> pre_scan -> merge -> segment-K2 (dense only) */
+#define KDA_MODE_SEGMENT 1  /* segment-parallel: pre_scan -> merge -> segment-K2 (dense or packed varlen) */
 #define KDA_MODE_AUTO 2     /* library picks serial or segment from the shape */
 
 typedef struct kda_options {
@@ -163,7 +163,8 @@ kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q
                                        float* final_state, int32_t segment_len, void* stream);
 
 /* Bytes of device workspace a call with this shape and these options uses
- * (0 for serial mode).  No device work, except that KDA_MODE_AUTO reads the current
+ * (0 for serial mode).  A shape with num_seqs > 0 is taken as packed varlen input
+ * (segment mode then sizes for at most num_seqs + seq_len / segment_len segments).  No device work, except that KDA_MODE_AUTO reads the current
  * device's resident cluster count to resolve the plan; *bytes is written on success. */
 kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, size_t* bytes);
 

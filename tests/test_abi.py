@@ -85,8 +85,8 @@ def test_varlen_rules(lib):
     assert _call(lib, KdaShape(2, 16, 1, 4, 128), cu=0x70000000) == INVALID  # batch != 1
     assert _call(lib, KdaShape(1, 16, 0, 4, 128), cu=0x70000000) == INVALID  # num_seqs 0
     assert _call(lib, KdaShape(1, 16, 1, 4, 128), cu=0x70000002) == INVALID  # misaligned
-    opts = KdaOptions(1, 64, 0, 0, 0)  # segment mode needs dense input
-    assert _call(lib, KdaShape(1, 16, 1, 4, 128), cu=0x70000000, opts=opts) == INVALID
+    opts = KdaOptions(1, 64, 0, 0, 0)  # segment mode accepts packed varlen input
+    assert _call(lib, KdaShape(1, 16, 1, 4, 128), cu=0x70000000, opts=opts) not in (INVALID, ALIAS)
 
 
 def test_options_rules(lib):
@@ -166,3 +166,14 @@ def test_planner_rejects_bad_arguments(lib):
         K.kda_plan(1, 1000, 4, 0)
     with pytest.raises(K.KdaError):
         K.kda_plan(1, 1000, 4, 76, head_dim=64)
+
+
+def test_varlen_segment_workspace_bound(lib):
+    # N sequences over T tokens have at most N + T / segment_len segments; three fp32
+    # 128 x 128 tables per (segment, head) plus the int32 segment table.
+    N, T, H, seg = 5, 1000, 3, 64
+    nb = K.kda_workspace_bytes(1, T, H, mode=K.MODE_SEGMENT, segment_len=seg, num_seqs=N)
+    rows = N + T // seg
+    assert nb == 256 + 3 * rows * H * 128 * 128 * 4
+    # a packed batch no longer than one segment runs serially
+    assert K.kda_workspace_bytes(1, 64, H, mode=K.MODE_SEGMENT, segment_len=64, num_seqs=3) == 0

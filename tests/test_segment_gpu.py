@@ -135,3 +135,59 @@ def test_auto_mode_plans_segments_for_few_chains(orc):
 
 def test_auto_mode_keeps_serial_for_many_chains():
     assert K.kda_workspace_bytes(1, 8192, 64, mode=K.MODE_AUTO) == 0
+
+
+def run_varlen(inp, mode, seg_len=0):
+    w = inp["workload"]
+    out, fin = K.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                             initial_state=inp["initial_state"], cu_seqlens=inp["cu_seqlens"],
+                             output_final_state=True, mode=mode, segment_len=seg_len)
+    torch.cuda.synchronize()
+    assert K.kda_get_device_status() == 0
+    return out.reshape(-1, w.num_heads, 128), fin
+
+
+@pytest.mark.parametrize("lens,seg", [
+    ([300, 17, 0, 129, 64], 64),      # ragged tails, an empty sequence, exact multiple
+    ([33, 1, 70, 256], 32),           # one-token sequence, many segments
+    ([500], 128),                     # a single packed sequence
+    ([16, 16, 16], 16),               # every sequence one segment
+])
+def test_varlen_segment_matches_oracle(orc, lens, seg):
+    inp = make_inputs(custom(lens, 3, True, seed=400 + sum(lens) + seg, dense=False), DEV)
+    out, fin = run_varlen(inp, K.MODE_SEGMENT, seg)
+    o_ref, f_ref = oracle_on_heads(orc, inp, range(3))
+    assert_close(gpu_out_heads(out, range(3)), o_ref, "varlen segment out")
+    assert_close(gpu_state_heads(fin, range(3)), f_ref, "varlen segment final")
+
+
+def test_varlen_segment_stress_slow_decay(orc):
+    inp = make_inputs(custom([700, 45, 260], 2, True, seed=411, dense=False), DEV, stress=True)
+    out, fin = run_varlen(inp, K.MODE_SEGMENT, 128)
+    o_ref, f_ref = oracle_on_heads(orc, inp, range(2))
+    assert_close(gpu_out_heads(out, range(2)), o_ref, "varlen segment stress out")
+    assert_close(gpu_state_heads(fin, range(2)), f_ref, "varlen segment stress final")
+
+
+def test_varlen_segment_workload_vs_serial(orc):
+    """The packed varlen workload (H = 12) in segment mode: oracle on sampled heads and the
+    max difference against serial mode."""
+    inp = make_inputs(WORKLOADS["varlen_h12"], DEV)
+    o_seg, f_seg = run_varlen(inp, K.MODE_SEGMENT, 1024)
+    o_ser, f_ser = run_varlen(inp, K.MODE_SERIAL)
+    heads = [0, 11]
+    o_ref, f_ref = oracle_on_heads(orc, inp, heads)
+    assert_close(gpu_out_heads(o_seg, heads), o_ref, "varlen_h12 segment out")
+    assert_close(gpu_state_heads(f_seg, heads), f_ref, "varlen_h12 segment final")
+    d_out = (o_seg.float() - o_ser.float()).abs().max().item()
+    print(f"\nvarlen segment vs serial max |diff|: out {d_out:.3e}")
+    assert d_out < 2e-2
+
+
+def test_varlen_segment_bad_cu_seqlens_is_reported():
+    inp = make_inputs(custom([100, 100, 100], 2, False, seed=412, dense=False), DEV)
+    bad = torch.tensor([0, 150, 120, 300], dtype=torch.int32, device=DEV)  # decreasing
+    K.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                  cu_seqlens=bad, mode=K.MODE_SEGMENT, segment_len=32)
+    assert K.kda_get_device_status() == 1
+    assert K.kda_get_device_status() == 0
