@@ -45,13 +45,19 @@ COMPUTE_DTYPE = "bf16"
 _FWD_SOURCES = ["chunked_kda_delta_gb300/csrc/kda_fwd_tc.cu",
                 "chunked_kda_delta_gb300/csrc/kda_ptx.cuh",
                 "chunked_kda_delta_gb300/csrc/kda_internal.cuh"]
+_DECODE_SOURCES = ["chunked_kda_delta_gb300/csrc/kda_decode.cu",
+                   "chunked_kda_delta_gb300/csrc/kda_internal.cuh"]
 KERNEL_SOURCES = {"serial": _FWD_SOURCES,
                   "segment": _FWD_SOURCES + ["chunked_kda_delta_gb300/csrc/kda_merge.cu"],
-                  "auto": _FWD_SOURCES + ["chunked_kda_delta_gb300/csrc/kda_merge.cu"]}
+                  "auto": _FWD_SOURCES + ["chunked_kda_delta_gb300/csrc/kda_merge.cu"],
+                  "decode_fp32": _DECODE_SOURCES, "decode_bf16": _DECODE_SOURCES}
 KERNEL_NAMES = {"serial": "kda_fwd_tc_kernel",
                 "segment": "kda_fwd_tc_kernel x3 + kda_merge_kernel (whole step)",
-                "auto": "the plan the library picks (whole step)"}
-LAUNCHES_PER_STEP = {"serial": 1, "segment": 4, "auto": 1}
+                "auto": "the plan the library picks (whole step)",
+                "decode_fp32": "kda_decode_kernel<float>",
+                "decode_bf16": "kda_decode_kernel<bf16>"}
+LAUNCHES_PER_STEP = {"serial": 1, "segment": 4, "auto": 1, "decode_fp32": 1, "decode_bf16": 1}
+DECODE_METRIC = "decode head-tokens/s (B·H/s) and % of roofline on 1 GB300"
 
 
 def parse_args():
@@ -63,6 +69,8 @@ def parse_args():
     ap.add_argument("--workload", default="single_t8192_h64")
     ap.add_argument("--mode", choices=["serial", "segment", "auto"], default="serial")
     ap.add_argument("--segment-len", type=int, default=0)
+    ap.add_argument("--state-dtype", choices=["fp32", "bf16"], default="fp32",
+                    help="state storage of a decode workload")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -75,9 +83,10 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
-def algorithmic_bytes(w) -> int:
+def algorithmic_bytes(w, state_elem: int = 4) -> int:
     states = (1 if w.has_initial_state else 0) + 1   # read S0 (if given) + write final
-    return BYTES_PER_HEAD_TOKEN * w.head_tokens + STATE_BYTES * w.num_seqs * w.num_heads * states
+    state_bytes = STATE_BYTES // 4 * state_elem
+    return BYTES_PER_HEAD_TOKEN * w.head_tokens + state_bytes * w.num_seqs * w.num_heads * states
 
 
 def measured_peaks():
@@ -284,7 +293,7 @@ def run_reference(args, w):
     desc = (f"{len(hs)} of {w.num_heads} heads x first {nt} of {w.total_tokens} tokens per step "
             f"(fp64 token-by-token recurrence)")
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "metric": DECODE_METRIC if w.decode else METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -310,6 +319,15 @@ def job_throughput(world: int, head_tokens_per_rank: int, steps: int, seconds: f
     return world * head_tokens_per_rank * steps / seconds
 
 
+def kind_of(w, args) -> str:
+    """The kernel set a run times: a prefill mode, or the decode step with its state type."""
+    return f"decode_{args.state_dtype}" if w.decode else args.mode
+
+
+def state_elem_of(w, args) -> int:
+    return 2 if (w.decode and args.state_dtype == "bf16") else 4
+
+
 def workload_config(w, args, note=None):
     cfg = {"workload": w.name, "seq_lens": (list(w.seq_lens) if len(w.seq_lens) <= 4 else
                                             f"{w.num_seqs} sequences, {w.total_tokens} tokens"),
@@ -322,7 +340,12 @@ def workload_config(w, args, note=None):
            "precision": "bf16 tensor-core operands, fp32 accumulation, fp32 state",
            "head_tokens_per_gpu": w.head_tokens, "parallelism": f"replicas x{args.gpus}",
            "l2": "no flush; inputs larger than L2 "
-                 f"({algorithmic_bytes(w) / 1e6:.0f} MB per step vs 129 MB)"}
+                 f"({algorithmic_bytes(w, state_elem_of(w, args)) / 1e6:.0f} MB per step vs 129 MB)"}
+    if w.decode:
+        cfg.update(mode="decode", segment_len=None, plan="decode",
+                   state_dtype=args.state_dtype, step="one decode token per sequence, "
+                   "state cache updated in place",
+                   precision=f"fp32 CUDA-core arithmetic, {args.state_dtype} state storage")
     if note:
         cfg["note"] = note
     return cfg
@@ -350,7 +373,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     mode = {"serial": K.MODE_SERIAL, "segment": K.MODE_SEGMENT, "auto": K.MODE_AUTO}[args.mode]
-    if args.mode == "auto":
+    if args.mode == "auto" and not w.decode:
         # what the library will pick (its resident-cluster count is the occupancy query;
         # one cluster per SM pair is the same on this part)
         props = torch.cuda.get_device_properties(dev)
@@ -358,16 +381,26 @@ def main():
                             w.num_heads, max(1, props.multi_processor_count // 2),
                             varlen=not w.dense, num_seqs=0 if w.dense else w.num_seqs)
         args.planned = ("segment", ps) if pm == K.MODE_SEGMENT else ("serial", 0)
+    kind = kind_of(w, args)
     inp, a, cu = device_inputs(K, w, dev)
     N = w.num_seqs
     out = torch.empty_like(a["q"])
     fin = torch.empty((N, w.num_heads, 128, 128), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        K.kda_prefill(**a, scale=inp["scale"], initial_state=inp["initial_state"], cu_seqlens=cu,
-                      out=out, final_state=fin, stream=stream, mode=mode,
-                      segment_len=args.segment_len)
+    if w.decode:
+        # a state cache resident in HBM, advanced in place by one token per sequence
+        cache = inp["initial_state"].to(torch.bfloat16 if args.state_dtype == "bf16"
+                                        else torch.float32)
+
+        def step():
+            K.kda_decode(**a, scale=inp["scale"], initial_state=cache, final_state=cache,
+                         out=out, stream=stream)
+    else:
+        def step():
+            K.kda_prefill(**a, scale=inp["scale"], initial_state=inp["initial_state"],
+                          cu_seqlens=cu, out=out, final_state=fin, stream=stream, mode=mode,
+                          segment_len=args.segment_len)
 
     clocks = ClockSampler(gpu_identifier(torch, dev))
     for _ in range(max(3, args.warmup)):
@@ -375,10 +408,10 @@ def main():
     torch.cuda.synchronize()
     if K.kda_get_device_status() != 0:
         raise RuntimeError("device status error after warm-up")
-    launches_per_step = LAUNCHES_PER_STEP.get(args.mode, 1)
-    if args.mode == "auto":
+    launches_per_step = LAUNCHES_PER_STEP.get(kind, 1)
+    if args.mode == "auto" and not w.decode:
         launches_per_step = 4 if args.planned[0] == "segment" else 1
-    if args.mode == "segment":
+    if args.mode == "segment" and not w.decode:
         seg = args.segment_len or 8192
         if w.dense and w.seq_lens[0] <= seg:
             launches_per_step = 1  # a single segment runs the plain serial pass
@@ -407,7 +440,33 @@ def main():
     value = job_throughput(world, w.head_tokens, args.steps, elapsed_ms / 1e3)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and w.decode:
+        # the token inputs come from pinned host memory and the outputs go back every
+        # step; the state cache stays resident on the device, as decoding keeps it
+        host = {k: a[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+        def e2e_step():
+            for key, x in host.items():
+                a[key].copy_(x, non_blocking=True)
+            K.kda_decode(**a, scale=inp["scale"], initial_state=cache, final_state=cache,
+                         out=out, stream=stream)
+            oh.copy_(out, non_blocking=True)
+            stream.synchronize()
+        e2e_step()
+        if pg:
+            pg.barrier()
+        t = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t) / args.e2e_steps
+        e2e_s = max_over_ranks([e2e_s], pg, dev)[0]
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
+        e2e = {"value": job_throughput(world, w.head_tokens, 1, e2e_s), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": oh.numel() * 2,
+               "ms_per_step": e2e_s * 1e3,
+               "note": "torch copies + kda_decode; the state cache stays on the device"}
+    elif not args.no_e2e:
         host = {k: inp[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
         s0h = None if inp["initial_state"] is None else inp["initial_state"].cpu().pin_memory()
         cuh = None if cu is None else cu.cpu()
@@ -443,11 +502,11 @@ def main():
 
     if rank == 0:
         peak, peak_kind = measured_peaks()
-        algo = algorithmic_bytes(w)
+        algo = algorithmic_bytes(w, state_elem_of(w, args))
         achieved = algo / (kernel_ms / 1e3) / 1e9
-        traffic = recorded_traffic(w.name, args.mode)
+        traffic = recorded_traffic(w.name, kind)
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "metric": DECODE_METRIC if w.decode else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": COMPUTE_DTYPE, "data": "synthetic",
@@ -455,7 +514,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
-                         "kernel": KERNEL_NAMES.get(args.mode, args.mode),
+                         "kernel": KERNEL_NAMES.get(kind, kind),
                          "kernel_ms": kernel_ms, "algorithmic_bytes_per_launch": algo},
             "cpu_baseline": cpu,
             "e2e": e2e,

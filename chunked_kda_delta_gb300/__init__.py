@@ -14,6 +14,9 @@ from .kda import (  # noqa: F401
     kda_release_workspaces,
     kda_workspace_bytes,
     kda_plan,
+    kda_decode,
+    STATE_F32,
+    STATE_BF16,
     load_library,
     MODE_SERIAL,
     MODE_SEGMENT,

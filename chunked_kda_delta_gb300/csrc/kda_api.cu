@@ -289,14 +289,14 @@ kda_status validate_options(const kda_options* o, const Problem& pr, int32_t* mo
 
 kda_status validate_pointers(const Problem& pr, const uint16_t* q, const uint16_t* k,
                              const uint16_t* v, const float* g, const uint16_t* beta, float scale,
-                             const float* s0, const int32_t* cu, const uint16_t* out,
-                             const float* sfin) {
+                             const void* s0, const int32_t* cu, const uint16_t* out,
+                             const void* sfin, size_t state_elem = 4) {
     if (!(scale == scale) || scale > 3.4e38f || scale < -3.4e38f)
         return fail(KDA_ERR_INVALID_ARGUMENT, "scale must be finite");
     const size_t x2 = (size_t)pr.T_total * pr.H * kda::kD * 2;
     const size_t x4 = x2 * 2;
     const size_t b2 = (size_t)pr.T_total * pr.H * 2;
-    const size_t st = (size_t)pr.N * pr.H * kda::kD * kda::kD * 4;
+    const size_t st = (size_t)pr.N * pr.H * kda::kD * kda::kD * state_elem;
     const size_t cub = pr.varlen ? (size_t)(pr.N + 1) * 4 : 0;
     if (pr.T_total > 0) {
         const void* req[] = {q, k, v, g, beta, out};
@@ -681,6 +681,45 @@ kda_status kda_plan(const kda_shape* shape, int32_t varlen, int32_t resident_clu
     kda_status st = validate_shape(shape, varlen != 0, &pr);
     if (st != KDA_OK) return st;
     choose_plan(pr, resident_clusters, mode, segment_len);
+    return KDA_OK;
+}
+
+kda_status kda_decode(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
+                      const uint16_t* v, const float* g, const uint16_t* beta, float scale,
+                      const void* initial_state, void* final_state, int32_t state_dtype,
+                      uint16_t* out, void* stream) {
+    t_last_error[0] = '\0';
+    Problem pr{};
+    kda_status st = validate_shape(shape, false, &pr);
+    if (st != KDA_OK) return st;
+    if (state_dtype != KDA_STATE_F32 && state_dtype != KDA_STATE_BF16)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "unknown state_dtype %d", state_dtype);
+    const size_t elem = state_dtype == KDA_STATE_BF16 ? 2 : 4;
+    if ((st = validate_pointers(pr, q, k, v, g, beta, scale, initial_state, nullptr, out,
+                                final_state, elem)) != KDA_OK)
+        return st;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo* di = nullptr;
+    if ((st = device_info(dev, &di)) != KDA_OK) return st;
+    if (pr.T_total == 0 && !final_state) return KDA_OK;
+    kda::DecodeParams p{};
+    p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16*>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16*>(v);
+    p.g = g;
+    p.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
+    p.s0 = initial_state;
+    p.sfin = final_state;
+    p.out = reinterpret_cast<__nv_bfloat16*>(out);
+    p.T = pr.dense_len;
+    p.N = pr.N;
+    p.H = pr.H;
+    p.scale = scale;
+    p.state_bf16 = state_dtype == KDA_STATE_BF16;
+    if ((e = kda::launch_decode(p, (cudaStream_t)stream)) != cudaSuccess)
+        return cuda_fail(e, "decode kernel launch");
     return KDA_OK;
 }
 

@@ -50,6 +50,23 @@ struct FwdParams {
     int32_t rows;         // varlen segment launches: rows launched (an upper bound)
 };
 
+// The recurrent decode step: T tokens of each of N dense sequences, H heads.
+struct DecodeParams {
+    const __nv_bfloat16* q;   // [N][T][H][128]
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* g;
+    const __nv_bfloat16* beta;  // [N][T][H]
+    const void* s0;           // [N][H][128][128] fp32 or bf16 (state_bf16), or nullptr
+    void* sfin;               // same layout and type, or nullptr; may equal s0
+    __nv_bfloat16* out;       // [N][T][H][128]
+    int64_t T;
+    int32_t N;
+    int32_t H;
+    float scale;
+    int32_t state_bf16;       // 1: states are bf16, else fp32
+};
+
 // Launch flags of the fused kernel.
 constexpr int32_t kFlagNoOutput = 1;       // no output rows (summary runs)
 constexpr int32_t kFlagZeroV = 2;          // treat v as zero (transition runs: U = 0)
@@ -127,6 +144,8 @@ cudaError_t launch_segment_table(const int32_t* cu, int32_t N, int64_t T_total, 
 cudaError_t launch_merge(const float* m_seg, const float* b_seg, const float* s0, float* carries,
                          int32_t B, int32_t nseg, int32_t H, cudaStream_t stream,
                          const int32_t* seg_start = nullptr);
+// Decode: one CTA per (sequence, head).
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 size_t serial_smem_bytes();
 int serial_block_threads();
 const void* serial_kernel_symbol();

@@ -42,6 +42,7 @@ class Workload:
     dense: bool              # True: equal lengths, passed as [B, T, H, D] without cu_seqlens
     seed: int
     head_dim: int = D_HEAD
+    decode: bool = False     # True: one decode step (kda_decode) per sequence, not a prefill
 
     @property
     def total_tokens(self) -> int:
@@ -72,6 +73,9 @@ WORKLOADS = {
     # the long-sequence distributions with few heads: too few chains to fill the GPU
     # serially, the case the segment planner exists for
     "long_t131072_h4": Workload("long_t131072_h4", (131072,), 4, False, True, 5),
+    # one decode step of a batch of 256 sequences over 64 heads (a state cache of
+    # 256 x 64 states: 1 GiB in fp32, larger than L2)
+    "decode_b256_h64": Workload("decode_b256_h64", (1,) * 256, 64, True, True, 6, decode=True),
 }
 
 

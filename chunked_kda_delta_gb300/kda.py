@@ -30,7 +30,12 @@ EXPORTED_SYMBOLS = (
     "kda_prefill", "kda_prefill_ex", "kda_prefill_host", "kda_workspace_bytes",
     "kda_get_device_status", "kda_release_workspaces", "kda_status_string",
     "kda_last_error_message", "kda_version", "kda_prefill_segment_noalloc", "kda_plan",
+    "kda_decode",
 )
+
+STATE_F32 = 0
+STATE_BF16 = 1
+_STATE_DTYPES = {torch.float32: STATE_F32, torch.bfloat16: STATE_BF16}
 
 
 class KdaError(RuntimeError):
@@ -85,6 +90,8 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False) -> 
                                             ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_plan.argtypes = [ctypes.POINTER(KdaShape), ctypes.c_int32, ctypes.c_int32,
                                  ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+        lib.kda_decode.argtypes = [ctypes.POINTER(KdaShape), u16p, u16p, u16p, f32p, u16p,
+                                   ctypes.c_float, vp, vp, ctypes.c_int32, u16p, vp]
         lib.kda_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         lib.kda_release_workspaces.argtypes = [ctypes.c_int32]
         lib.kda_status_string.argtypes = [ctypes.c_int]
@@ -92,7 +99,7 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False) -> 
         lib.kda_last_error_message.restype = ctypes.c_char_p
         lib.kda_version.restype = ctypes.c_char_p
         for f in (lib.kda_prefill, lib.kda_prefill_ex, lib.kda_prefill_host,
-                  lib.kda_prefill_segment_noalloc,
+                  lib.kda_prefill_segment_noalloc, lib.kda_decode,
                   lib.kda_workspace_bytes, lib.kda_get_device_status, lib.kda_plan,
                   lib.kda_release_workspaces):
             f.restype = ctypes.c_int
@@ -321,3 +328,56 @@ def kda_prefill_segment_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
             int(segment_len), ctypes.c_void_p(int(stream)))
     _check(lib, st)
     return out, final_state
+
+
+def kda_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+               beta: torch.Tensor, scale: Optional[float] = None,
+               initial_state: Optional[torch.Tensor] = None,
+               final_state: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None, output_final_state: bool = True,
+               state_dtype: Optional[torch.dtype] = None, stream=None):
+    """The recurrent decode step on CUDA tensors; returns ``(out, final_state)``.
+
+    q, k, v: bf16 ``[B, H, 128]`` (one token per sequence) or ``[B, T, H, 128]``;
+    g: fp32 of the same shape; beta: bf16 ``[B, H]`` or ``[B, T, H]``.  States are
+    ``[B, H, 128, 128]`` in fp32 or bf16 (``state_dtype``, else the dtype of the
+    state tensors given, else fp32).  Pass ``final_state = initial_state`` to update a
+    state cache in place; a new final state is allocated when ``output_final_state``
+    is set and none is given.
+    """
+    lib = load_library()
+    single = q.dim() == 3
+    if single:
+        q, k, v, g = (x.unsqueeze(1) for x in (q, k, v, g))
+        beta = beta.unsqueeze(1)
+    _check_tensors(q, k, v, g, beta, None, None, "cuda")
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, 128] or [B, T, H, 128]")
+    B, T, H, D = q.shape
+    given = [t for t in (initial_state, final_state) if t is not None]
+    if state_dtype is None:
+        state_dtype = given[0].dtype if given else torch.float32
+    if state_dtype not in _STATE_DTYPES:
+        raise ValueError("state_dtype must be torch.float32 or torch.bfloat16")
+    for t in given:
+        if t.dtype != state_dtype or not t.is_contiguous() or t.device.type != "cuda":
+            raise ValueError(f"states must be contiguous {state_dtype} CUDA tensors")
+        if tuple(t.shape) != (B, H, D, D):
+            raise ValueError(f"states must be [{B}, {H}, {D}, {D}]")
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((B, H, D, D), dtype=state_dtype, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    shape = KdaShape(B, T, 0, H, D)
+    with torch.cuda.device(q.device):
+        st = lib.kda_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                            ctypes.c_float(scale), _ptr(initial_state), _ptr(final_state),
+                            _STATE_DTYPES[state_dtype], _ptr(out), ctypes.c_void_p(int(stream)))
+    _check(lib, st)
+    return (out.squeeze(1) if single else out), final_state

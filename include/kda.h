@@ -162,6 +162,42 @@ kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q
                                        const float* initial_state, uint16_t* out,
                                        float* final_state, int32_t segment_len, void* stream);
 
+/* State storage types of kda_decode. */
+#define KDA_STATE_F32 0   /* fp32 [N][H][128][128] */
+#define KDA_STATE_BF16 1  /* bf16 [N][H][128][128]; arithmetic stays fp32, rounded on store */
+
+/* kda_decode -- the recurrent step for a few tokens (typically one) of each sequence,
+ * the inner step of autoregressive decoding: per (sequence, head) and token, the
+ * recurrence at the top of this header (cuLA PR #103 "feat(kda/sm90): FlashKDA
+ * prefill port + intracard-CP prefill", problem statement), applied token by token to
+ * a state that stays resident on the device.  The pages mention a decode registration
+ * beside the prefill (flashinfer PR #4313 "feat(cake_kda): share recurrent prefill
+ * kernels across SM100 family", publication notes) and a bf16 final state in the
+ * reference facade (flashinfer PR #4351 review of kda_prefill.py); neither gives the
+ * kernel, so this one is the recurrence itself, HBM-bound on the state.
+ *   shape          dense only: batch = N sequences, seq_len = T tokens of each
+ *                  (T >= 0; the cost grows linearly in T, use kda_prefill for long
+ *                  inputs), num_seqs ignored, head_dim 128, num_heads >= 1
+ *   q, k, v, g     device, layouts as kda_prefill ([N][T][H][128]); may be NULL only
+ *                  when N * T == 0
+ *   beta           device bf16 [N][T][H]
+ *   scale          output scale (finite)
+ *   initial_state  device [N][H][128][128] of state_dtype, or NULL (zero state)
+ *   final_state    device, same layout and type, or NULL (not written); may be the very
+ *                  same pointer as initial_state (the usual in-place update of a state
+ *                  cache) but must not otherwise overlap it or any input
+ *   state_dtype    KDA_STATE_F32 or KDA_STATE_BF16, for both state pointers
+ *   out            device bf16 [N][T][H][128]; must not overlap any other argument
+ * Alignment as kda_prefill (16 bytes for every tensor but beta).  Asynchronous on
+ * `stream`; no workspace, no device status word.  T == 0 copies (or zero-fills, with
+ * no initial state) the state; with T == 0 and no final state it is a no-op.
+ * Errors: KDA_ERR_INVALID_ARGUMENT (shape, pointer, state_dtype), KDA_ERR_ALIASING,
+ * KDA_ERR_UNSUPPORTED_DEVICE, KDA_ERR_CUDA (launch). */
+kda_status kda_decode(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
+                      const uint16_t* v, const float* g, const uint16_t* beta, float scale,
+                      const void* initial_state, void* final_state, int32_t state_dtype,
+                      uint16_t* out, void* stream);
+
 /* Bytes of device workspace a call with this shape and these options uses
  * (0 for serial mode).  A shape with num_seqs > 0 is taken as packed varlen input
  * (segment mode then sizes for at most num_seqs + seq_len / segment_len segments).  No device work, except that KDA_MODE_AUTO reads the current

@@ -177,3 +177,40 @@ def test_varlen_segment_workspace_bound(lib):
     assert nb == 256 + 3 * rows * H * 128 * 128 * 4
     # a packed batch no longer than one segment runs serially
     assert K.kda_workspace_bytes(1, 64, H, mode=K.MODE_SEGMENT, segment_len=64, num_seqs=3) == 0
+
+
+def _decode(lib, shape, state_dtype=0, scale=0.1, **over):
+    base = dict(q=0x10000000, k=0x20000000, v=0x30000000, g=0x40000000, beta=0x50000000,
+                s0=None, fin=None, out=0x60000000)
+    base.update(over)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return lib.kda_decode(ctypes.byref(shape), P(base["q"]), P(base["k"]), P(base["v"]),
+                          P(base["g"]), P(base["beta"]), ctypes.c_float(scale), P(base["s0"]),
+                          P(base["fin"]), int(state_dtype), P(base["out"]), None)
+
+
+def test_decode_validation(lib):
+    s = KdaShape(8, 1, 0, 4, 128)
+    assert _decode(lib, s, state_dtype=2) == INVALID
+    assert _decode(lib, s, state_dtype=-1) == INVALID
+    assert _decode(lib, KdaShape(8, 1, 0, 4, 64)) == INVALID
+    assert _decode(lib, s, q=None) == INVALID
+    assert _decode(lib, s, s0=0x70000008) == INVALID                 # not 16-byte aligned
+    assert _decode(lib, s, scale=float("nan")) == INVALID
+    # out inside q; final state inside an input
+    assert _decode(lib, s, out=0x10000000 + 64) == ALIAS
+    assert _decode(lib, s, fin=0x20000000) == ALIAS
+    # a bf16 state is half the bytes: states 32 KiB apart are disjoint in bf16 only
+    st16 = 8 * 4 * 128 * 128 * 2
+    assert _decode(lib, s, state_dtype=1, s0=0x70000000, fin=0x70000000 + st16) not in (INVALID, ALIAS)
+    assert _decode(lib, s, state_dtype=0, s0=0x70000000, fin=0x70000000 + st16) == ALIAS
+    # exact in-place alias is accepted (without a GPU the next step fails in CUDA)
+    assert _decode(lib, s, state_dtype=1, s0=0x70000000, fin=0x70000000) not in (INVALID, ALIAS)
+
+
+def test_decode_binding_checks_state_dtype():
+    q = torch.zeros(2, 3, 128, dtype=torch.bfloat16)
+    g = torch.zeros(2, 3, 128, dtype=torch.float32)
+    b = torch.zeros(2, 3, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # CPU tensors are refused before any library call
+        K.kda_decode(q, q, q, g, b, initial_state=torch.zeros(2, 3, 128, 128))
