@@ -43,8 +43,8 @@
  * conditions (malformed cu_seqlens contents, a bounded wait that ran out) are
  * recorded in a per-device status word read by kda_get_device_status().
  *
- * Asynchrony: kda_prefill / kda_prefill_ex enqueue work on `stream` and return
- * without synchronising.  `stream` is a cudaStream_t passed as void* (NULL =
+ * Asynchrony: kda_prefill, kda_prefill_ex and kda_decode enqueue work on `stream` and
+ * return without synchronising.  `stream` is a cudaStream_t passed as void* (NULL =
  * the legacy default stream).  The current CUDA device must own all pointers.
  */
 #ifndef KDA_H_
@@ -118,8 +118,8 @@ kda_status kda_prefill(const kda_shape* shape, const uint16_t* q, const uint16_t
                        float* final_state, void* stream);
 
 /* kda_prefill_ex -- kda_prefill with options (mode, segment length, wait limit).
- * opts == NULL behaves as kda_prefill.  Segment mode requires dense input;
- * segment_len must be a positive multiple of 16. */
+ * opts == NULL behaves as kda_prefill.  Segment mode takes dense or packed varlen
+ * input; segment_len must be a positive multiple of 16. */
 kda_status kda_prefill_ex(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
                           const uint16_t* v, const float* g, const uint16_t* beta, float scale,
                           const float* initial_state, const int32_t* cu_seqlens, uint16_t* out,
@@ -164,7 +164,8 @@ kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q
 
 /* State storage types of kda_decode. */
 #define KDA_STATE_F32 0   /* fp32 [N][H][128][128] */
-#define KDA_STATE_BF16 1  /* bf16 [N][H][128][128]; arithmetic stays fp32, rounded on store */
+#define KDA_STATE_BF16 1  /* bf16 [N][H][128][128]; arithmetic stays fp32, the state is
+                             rounded to bf16 (nearest even) after every token */
 
 /* kda_decode -- the recurrent step for a few tokens (typically one) of each sequence,
  * the inner step of autoregressive decoding: per (sequence, head) and token, the
