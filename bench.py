@@ -84,9 +84,13 @@ def dist_env():
 
 
 def algorithmic_bytes(w, state_elem: int = 4) -> int:
+    """Bytes a step must move: every input once, the output once, the states once each
+    way.  Per token: q and k rows of their own head counts, v, g and beta per state head,
+    out per output head (equal heads: BYTES_PER_HEAD_TOKEN per head)."""
     states = (1 if w.has_initial_state else 0) + 1   # read S0 (if given) + write final
     state_bytes = STATE_BYTES // 4 * state_elem
-    return BYTES_PER_HEAD_TOKEN * w.head_tokens + state_bytes * w.num_seqs * w.num_heads * states
+    per_token = 256 * (w.q_heads + w.k_heads + w.num_heads + w.out_heads) + 514 * w.num_heads
+    return per_token * w.total_tokens + state_bytes * w.num_seqs * w.num_heads * states
 
 
 def measured_peaks():
@@ -214,7 +218,7 @@ def device_inputs(K, w, dev):
     if w.dense:
         B, T = w.num_seqs, w.seq_lens[0]
         for key in ("q", "k", "v", "g"):
-            args[key] = args[key].view(B, T, w.num_heads, 128)
+            args[key] = args[key].view(B, T, args[key].shape[1], 128)
         args["beta"] = args["beta"].view(B, T, w.num_heads)
         cu = None
     else:
@@ -222,10 +226,25 @@ def device_inputs(K, w, dev):
     return inp, args, cu
 
 
+def oracle_head_args(w, inp, out_heads, rows=None):
+    """fp64 oracle inputs for the given OUTPUT heads (each run as a plain head on the q, k
+    and state heads it reads), restricted to token rows `rows` if given."""
+    import oracle
+    from chunked_kda_delta_gb300.inputs import to_f64_numpy
+    maps = [oracle.grouped_heads(ho, w.num_heads, w.q_heads) for ho in out_heads]
+    pick = {"q": [m[0] for m in maps], "k": [m[1] for m in maps]}
+    sx = [m[2] for m in maps]
+    d = {}
+    for key in ("q", "k", "v", "g", "beta"):
+        t = inp[key] if rows is None else inp[key][rows]
+        d[key] = to_f64_numpy(t[:, pick.get(key, sx)])
+    s0 = None if inp["initial_state"] is None else to_f64_numpy(inp["initial_state"][:, sx])
+    return d, s0
+
+
 def cpu_baseline(w, inp, seconds: float):
     """The fp64 oracle on the host cores, over a bounded sample of the workload's heads."""
     import oracle
-    from chunked_kda_delta_gb300.inputs import to_f64_numpy
     lib = oracle.default()
     cores = lib.max_threads()
     cu = inp["cu_seqlens"].cpu().numpy().astype("int64")
@@ -233,19 +252,18 @@ def cpu_baseline(w, inp, seconds: float):
     # short (a decode step takes well under a second), until `seconds`, or 3 s after at
     # least one full pass.
     done_heads, head_tokens, elapsed = 0, 0, 0.0
-    while elapsed < seconds and (done_heads < w.num_heads or elapsed < min(3.0, seconds)):
-        h0 = done_heads % w.num_heads
-        hs = list(range(h0, min(w.num_heads, h0 + cores)))
-        sel = {k: to_f64_numpy(inp[k][:, hs]) for k in ("q", "k", "v", "g", "beta")}
-        s0 = None if inp["initial_state"] is None else to_f64_numpy(inp["initial_state"][:, hs])
+    while elapsed < seconds and (done_heads < w.out_heads or elapsed < min(3.0, seconds)):
+        h0 = done_heads % w.out_heads
+        hs = list(range(h0, min(w.out_heads, h0 + cores)))
+        sel, s0 = oracle_head_args(w, inp, hs)
         t = time.perf_counter()
         lib.recurrent(sel["q"], sel["k"], sel["v"], sel["g"], sel["beta"], inp["scale"], s0=s0,
                       cu_seqlens=cu)
         elapsed += time.perf_counter() - t
         done_heads += len(hs)
         head_tokens += w.total_tokens * len(hs)
-    what = (f"{done_heads} of {w.num_heads} heads" if done_heads <= w.num_heads else
-            f"{done_heads / w.num_heads:.1f} passes over all {w.num_heads} heads")
+    what = (f"{done_heads} of {w.out_heads} heads" if done_heads <= w.out_heads else
+            f"{done_heads / w.out_heads:.1f} passes over all {w.out_heads} heads")
     return {"value": head_tokens / elapsed, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{what} x all {w.total_tokens} tokens "
                       f"(fp64 token-by-token recurrence, {elapsed:.1f} s)"}
@@ -258,14 +276,14 @@ def run_reference(args, w):
         return
     import numpy as np
     import oracle
-    from chunked_kda_delta_gb300.inputs import make_inputs, to_f64_numpy
+    from chunked_kda_delta_gb300.inputs import make_inputs
     lib = oracle.default()
     cores = lib.max_threads()
     # Inputs for a prefix of every head (the recurrence cost is the same for every token).
     budget = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
     probe_tokens = min(w.seq_lens[0] if w.seq_lens[0] > 0 else 1, 256)
     inp = make_inputs(w, "cpu")
-    hs = list(range(min(w.num_heads, cores)))
+    hs = list(range(min(w.out_heads, cores)))
     def sample(tokens):
         lens = []
         left = tokens
@@ -276,8 +294,7 @@ def run_reference(args, w):
         idx = np.concatenate([np.arange(c, c + t) for c, t in
                               zip(np.cumsum([0] + list(w.seq_lens[:-1])), lens)])
         cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
-        d = {k: to_f64_numpy(inp[k][idx][:, hs]) for k in ("q", "k", "v", "g", "beta")}
-        s0 = None if inp["initial_state"] is None else to_f64_numpy(inp["initial_state"][:, hs])
+        d, s0 = oracle_head_args(w, inp, hs, rows=idx)
         return d, s0, cu, sum(lens)
     d, s0, cu, nt = sample(probe_tokens)
     t = time.perf_counter()
@@ -296,7 +313,7 @@ def run_reference(args, w):
     total = time.perf_counter() - t
     ht = nt * len(hs)
     value = ht * args.steps / total
-    desc = (f"{len(hs)} of {w.num_heads} heads x first {nt} of {w.total_tokens} tokens per step "
+    desc = (f"{len(hs)} of {w.out_heads} heads x first {nt} of {w.total_tokens} tokens per step "
             f"(fp64 token-by-token recurrence)")
     print(json.dumps({
         "impl": "reference", "metric": DECODE_METRIC if w.decode else METRIC, "value": value, "unit": UNIT,
@@ -337,7 +354,7 @@ def state_elem_of(w, args) -> int:
 def workload_config(w, args, note=None):
     cfg = {"workload": w.name, "seq_lens": (list(w.seq_lens) if len(w.seq_lens) <= 4 else
                                             f"{w.num_seqs} sequences, {w.total_tokens} tokens"),
-           "num_heads": w.num_heads, "head_dim": 128, "chunk": 16,
+           "num_heads": w.num_heads, "num_q_heads": w.q_heads, "head_dim": 128, "chunk": 16,
            "initial_state": w.has_initial_state, "final_state": True, "mode": args.mode,
            "segment_len": ((args.segment_len or 8192) if args.mode == "segment" else
                            (getattr(args, "planned", ("serial", 0))[1] or None) if args.mode == "auto"
@@ -390,7 +407,7 @@ def main():
     kind = kind_of(w, args)
     inp, a, cu = device_inputs(K, w, dev)
     N = w.num_seqs
-    out = torch.empty_like(a["q"])
+    out = torch.empty(tuple(a["q"].shape[:-2]) + (w.out_heads, 128), dtype=torch.bfloat16, device=dev)
     fin = torch.empty((N, w.num_heads, 128, 128), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -479,9 +496,9 @@ def main():
         if w.dense:
             B, T = w.num_seqs, w.seq_lens[0]
             for key in ("q", "k", "v", "g"):
-                host[key] = host[key].view(B, T, w.num_heads, 128)
+                host[key] = host[key].view(B, T, host[key].shape[1], 128)
             host["beta"] = host["beta"].view(B, T, w.num_heads)
-        oh = torch.empty(host["q"].shape, dtype=torch.bfloat16).pin_memory()
+        oh = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
         fh = torch.empty((N, w.num_heads, 128, 128), dtype=torch.float32).pin_memory()
 
         def e2e_step():

@@ -72,6 +72,10 @@ kda_status device_info(int dev, DeviceInfo** out) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kda::serial_smem_bytes())))
             return cuda_fail(e, "cudaFuncSetAttribute(serial kernel)");
+        if ((e = cudaFuncSetAttribute(kda::grouped_kernel_symbol(),
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kda::serial_smem_bytes())))
+            return cuda_fail(e, "cudaFuncSetAttribute(grouped kernel)");
         if ((e = cudaFuncSetAttribute(kda::merge_kernel_symbol(),
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kda::merge_smem_bytes())))
@@ -222,9 +226,20 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 struct Problem {
     int64_t T_total, dense_len;
-    int32_t N, H;
+    int32_t N, H;        // H: heads of v, g, beta and the states
+    int32_t Hq, Hk, Ho;  // heads of q, of k (min(Hq, H)) and of the output (max(Hq, H))
     bool varlen;
 };
+
+// Bytes of each tensor of a problem (states in elements of `state_elem` bytes).
+struct Sizes {
+    size_t q, k, v, g, beta, out, state;
+};
+Sizes sizes_of(const Problem& pr, size_t state_elem = 4) {
+    const size_t t = (size_t)pr.T_total * kda::kD;
+    return {t * pr.Hq * 2, t * pr.Hk * 2, t * pr.H * 2, t * pr.H * 4, (size_t)pr.T_total * pr.H * 2,
+            t * pr.Ho * 2, (size_t)pr.N * pr.H * kda::kD * kda::kD * state_elem};
+}
 
 kda_status validate_shape(const kda_shape* s, bool varlen, Problem* pr) {
     if (!s) return fail(KDA_ERR_INVALID_ARGUMENT, "shape is NULL");
@@ -236,6 +251,13 @@ kda_status validate_shape(const kda_shape* s, bool varlen, Problem* pr) {
         return fail(KDA_ERR_INVALID_ARGUMENT, "seq_len must be >= 0 (got %lld)",
                     (long long)s->seq_len);
     pr->H = s->num_heads;
+    pr->Hq = s->num_q_heads ? s->num_q_heads : s->num_heads;
+    if (pr->Hq < 0 || (pr->Hq % pr->H != 0 && pr->H % pr->Hq != 0))
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "num_q_heads (%d) and num_heads (%d) must divide one another",
+                    s->num_q_heads, s->num_heads);
+    pr->Hk = pr->Hq < pr->H ? pr->Hq : pr->H;
+    pr->Ho = pr->Hq > pr->H ? pr->Hq : pr->H;
     pr->varlen = varlen;
     if (varlen) {
         if (s->batch != 1)
@@ -256,10 +278,10 @@ kda_status validate_shape(const kda_shape* s, bool varlen, Problem* pr) {
             return fail(KDA_ERR_INVALID_ARGUMENT, "seq_len too large");
         pr->T_total = (int64_t)s->batch * s->seq_len;
     }
-    if ((int64_t)pr->N * pr->H > 0x7fffffffll)
-        return fail(KDA_ERR_INVALID_ARGUMENT, "num_seqs * num_heads exceeds 2^31 - 1");
-    if (pr->T_total > ((int64_t)1 << 46) / ((int64_t)pr->H * kda::kD))
-        return fail(KDA_ERR_INVALID_ARGUMENT, "T_total * H * 128 is too large");
+    if ((int64_t)pr->N * pr->Ho > 0x3fffffffll)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "num_seqs * max(num_heads, num_q_heads) exceeds 2^30 - 1");
+    if (pr->T_total > ((int64_t)1 << 46) / ((int64_t)pr->Ho * kda::kD))
+        return fail(KDA_ERR_INVALID_ARGUMENT, "T_total * heads * 128 is too large");
     return KDA_OK;
 }
 
@@ -281,6 +303,9 @@ kda_status validate_options(const kda_options* o, const Problem& pr, int32_t* mo
                     "segment_len must be a non-negative multiple of 16 (got %d)", o->segment_len);
     if (o->wait_limit < 0)
         return fail(KDA_ERR_INVALID_ARGUMENT, "wait_limit must be >= 0");
+    if (o->mode == KDA_MODE_SEGMENT && pr.Hq != pr.H)
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "segment mode needs num_q_heads == num_heads (grouped heads run serially)");
     *mode = o->mode;
     if (o->segment_len) *seg_len = o->segment_len;
     if (o->wait_limit) *wait_limit = o->wait_limit;
@@ -293,10 +318,7 @@ kda_status validate_pointers(const Problem& pr, const uint16_t* q, const uint16_
                              const void* sfin, size_t state_elem = 4) {
     if (!(scale == scale) || scale > 3.4e38f || scale < -3.4e38f)
         return fail(KDA_ERR_INVALID_ARGUMENT, "scale must be finite");
-    const size_t x2 = (size_t)pr.T_total * pr.H * kda::kD * 2;
-    const size_t x4 = x2 * 2;
-    const size_t b2 = (size_t)pr.T_total * pr.H * 2;
-    const size_t st = (size_t)pr.N * pr.H * kda::kD * kda::kD * state_elem;
+    const Sizes sz = sizes_of(pr, state_elem);
     const size_t cub = pr.varlen ? (size_t)(pr.N + 1) * 4 : 0;
     if (pr.T_total > 0) {
         const void* req[] = {q, k, v, g, beta, out};
@@ -317,8 +339,8 @@ kda_status validate_pointers(const Problem& pr, const uint16_t* q, const uint16_
     if (sfin && !aligned(sfin, 16))
         return fail(KDA_ERR_INVALID_ARGUMENT, "final_state must be 16-byte aligned");
 
-    const Range rq{q, x2}, rk{k, x2}, rv{v, x2}, rg{g, x4}, rb{beta, b2}, rs0{s0, st},
-        rcu{cu, cub}, rout{out, x2}, rfin{sfin, st};
+    const Range rq{q, sz.q}, rk{k, sz.k}, rv{v, sz.v}, rg{g, sz.g}, rb{beta, sz.beta},
+        rs0{s0, sz.state}, rcu{cu, cub}, rout{out, sz.out}, rfin{sfin, sz.state};
     const Range ins[] = {rq, rk, rv, rg, rb, rs0, rcu, rfin};
     const char* in_names[] = {"q", "k", "v", "g", "beta", "initial_state", "cu_seqlens",
                               "final_state"};
@@ -358,7 +380,7 @@ constexpr size_t kPlanWorkspaceCap = (size_t)4 << 30;
 void choose_plan(const Problem& pr, int64_t resident, int32_t* mode, int32_t* seg_len) {
     *mode = KDA_MODE_SERIAL;
     *seg_len = 0;
-    if (pr.varlen || pr.dense_len <= 0) return;
+    if (pr.varlen || pr.dense_len <= 0 || pr.Hq != pr.H) return;
     const int64_t C = (int64_t)pr.N * pr.H;
     const int64_t R = resident > 0 ? resident : 1;
     auto cdiv = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
@@ -446,6 +468,7 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
     p.dense_len = pr.dense_len;
     p.N = pr.N;
     p.H = pr.H;
+    p.Hq = pr.Hq;
     p.scale = scale;
     p.wait_limit = wait_limit;
     p.debug_flags = debug_flags;
@@ -453,11 +476,11 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
     kda::TensorMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (pr.T_total > 0) {
-        if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "q")) ||
-            (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "k")) ||
+        if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hq, "q")) ||
+            (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hk, "k")) ||
             (st = encode_chunk_map(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "v")) ||
             (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")) ||
-            (st = encode_chunk_map(&maps.out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "out")))
+            (st = encode_chunk_map(&maps.out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Ho, "out")))
             return st;
     }
     if (mode == KDA_MODE_AUTO) choose_plan(pr, di->resident_clusters, &mode, &seg_len);
@@ -599,16 +622,14 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
             if (cu_seqlens[n + 1] < cu_seqlens[n])
                 return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must be non-decreasing");
     }
-    const size_t x2 = (size_t)pr.T_total * pr.H * kda::kD * 2;
-    const size_t x4 = x2 * 2;
-    const size_t b2 = (size_t)pr.T_total * pr.H * 2;
-    const size_t sb = (size_t)pr.N * pr.H * kda::kD * kda::kD * 4;
+    const Sizes sz = sizes_of(pr);
+    const size_t sb = sz.state;
     const size_t cub = pr.varlen ? (size_t)(pr.N + 1) * 4 : 0;
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    const size_t off_q = 0, off_k = off_q + up(x2), off_v = off_k + up(x2), off_g = off_v + up(x2),
-                 off_b = off_g + up(x4), off_s0 = off_b + up(b2),
+    const size_t off_q = 0, off_k = off_q + up(sz.q), off_v = off_k + up(sz.k),
+                 off_g = off_v + up(sz.v), off_b = off_g + up(sz.g), off_s0 = off_b + up(sz.beta),
                  off_cu = off_s0 + (initial_state ? up(sb) : 0), off_out = off_cu + up(cub),
-                 off_fin = off_out + up(x2), total = off_fin + (final_state ? up(sb) : 0);
+                 off_fin = off_out + up(sz.out), total = off_fin + (final_state ? up(sb) : 0);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -622,8 +643,8 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
         void* dst;
         const void* src;
         size_t n;
-    } ins[] = {{b + off_q, q, x2},  {b + off_k, k, x2},  {b + off_v, v, x2},
-               {b + off_g, g, x4},  {b + off_b, beta, b2},
+    } ins[] = {{b + off_q, q, sz.q},  {b + off_k, k, sz.k},  {b + off_v, v, sz.v},
+               {b + off_g, g, sz.g},  {b + off_b, beta, sz.beta},
                {b + off_s0, initial_state, initial_state ? sb : 0},
                {b + off_cu, cu_seqlens, cub}};
     for (auto& c : ins)
@@ -638,7 +659,7 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
              pr.varlen ? reinterpret_cast<int32_t*>(b + off_cu) : nullptr, d_out, d_fin, stream,
              mode, seg_len, wait_limit, debug_flags);
     if (st != KDA_OK) return st;
-    if (x2 && (e = cudaMemcpyAsync(out, d_out, x2, cudaMemcpyDeviceToHost, stream)))
+    if (sz.out && (e = cudaMemcpyAsync(out, d_out, sz.out, cudaMemcpyDeviceToHost, stream)))
         return cuda_fail(e, "cudaMemcpyAsync device->host (out)");
     if (d_fin && (e = cudaMemcpyAsync(final_state, d_fin, sb, cudaMemcpyDeviceToHost, stream)))
         return cuda_fail(e, "cudaMemcpyAsync device->host (final_state)");
@@ -716,6 +737,7 @@ kda_status kda_decode(const kda_shape* shape, const uint16_t* q, const uint16_t*
     p.T = pr.dense_len;
     p.N = pr.N;
     p.H = pr.H;
+    p.Hq = pr.Hq;
     p.scale = scale;
     p.state_bf16 = state_dtype == KDA_STATE_BF16;
     if ((e = kda::launch_decode(p, (cudaStream_t)stream)) != cudaSuccess)
@@ -840,6 +862,9 @@ extern "C" kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const 
     Problem pr{};
     kda_status st = validate_shape(shape, false, &pr);
     if (st != KDA_OK) return st;
+    if (pr.Hq != pr.H)
+        return fail(KDA_ERR_INVALID_ARGUMENT,
+                    "segment mode needs num_q_heads == num_heads (grouped heads run serially)");
     if (segment_len <= 0 || segment_len % kda::kChunk != 0)
         return fail(KDA_ERR_INVALID_ARGUMENT,
                     "segment_len must be a positive multiple of 16 (got %d)", segment_len);
@@ -875,17 +900,18 @@ extern "C" kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const 
     p.dense_len = pr.dense_len;
     p.N = pr.N;
     p.H = pr.H;
+    p.Hq = pr.Hq;
     p.scale = scale;
     p.wait_limit = kDefaultWaitLimit;
     p.status = di->status;
     kda::TensorMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (pr.T_total > 0) {
-        if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "q")) ||
-            (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "k")) ||
+        if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hq, "q")) ||
+            (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hk, "k")) ||
             (st = encode_chunk_map(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "v")) ||
             (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")) ||
-            (st = encode_chunk_map(&maps.out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "out")))
+            (st = encode_chunk_map(&maps.out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Ho, "out")))
             return st;
     }
     if (sp.nseg <= 1) {  // one segment: the plain serial pass, no scratch

@@ -37,11 +37,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_kernel(const Decode
     __shared__ float s_qk[kDecThreads / 32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t nh = blockIdx.x;
-    const int64_t n = nh / p.H;
-    const int h = (int)(nh % p.H);
+    const int Ho = p.Hq > p.H ? p.Hq : p.H, Hk = p.Hq > p.H ? p.H : p.Hq;
+    const int64_t n = (int64_t)blockIdx.x / Ho;
+    const int ho = (int)(blockIdx.x % Ho);
+    const HeadMap hm = head_map(ho, p.H, p.Hq);
     const int r0 = warp * kDecRows, c0 = lane * 4;
-    const size_t soff = (size_t)nh * kD * kD + (size_t)r0 * kD + c0;
+    const size_t soff = ((size_t)n * p.H + hm.hs) * kD * kD + (size_t)r0 * kD + c0;
 
     float s[kDecRows][4];
     if (p.s0) {
@@ -53,18 +54,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_kernel(const Decode
         for (int r = 0; r < kDecRows; ++r) s[r][0] = s[r][1] = s[r][2] = s[r][3] = 0.f;
     }
 
-    // Row (token t, head h) of sequence n starts at element (n T + t) H + h.  Threads
-    // 0..127 stage one channel each of the token's q, k, v and exp(g).
-    const size_t row0 = (size_t)n * p.T * p.H + h;
+    // Token t of sequence n is token n T + t; a tensor with X heads holds head x of it at
+    // row (n T + t) X + x.  Threads 0..127 stage one channel each of q, k, v and exp(g).
     for (int64_t t = 0; t < p.T; ++t) {
-        const size_t row = row0 + (size_t)t * p.H;
+        const size_t tok = (size_t)n * p.T + t;
+        const size_t row = tok * p.H + hm.hs;
         float beta_t = 0.f;
         if (tid < kD) {
-            const size_t e = row * kD + tid;
-            s_k[tid] = __bfloat162float(p.k[e]);
-            s_q[tid] = __bfloat162float(p.q[e]);
-            s_v[tid] = __bfloat162float(p.v[e]);
-            s_e[tid] = expf(p.g[e]);
+            s_k[tid] = __bfloat162float(p.k[(tok * Hk + hm.hk) * kD + tid]);
+            s_q[tid] = __bfloat162float(p.q[(tok * p.Hq + hm.hq) * kD + tid]);
+            s_v[tid] = __bfloat162float(p.v[row * kD + tid]);
+            s_e[tid] = expf(p.g[row * kD + tid]);
             beta_t = __bfloat162float(p.beta[row]);
         }
         __syncthreads();
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_kernel(const Decode
             }
             const float d = beta_t * (s_v[tid] - uu);
             s_d[tid] = d;
-            p.out[row * kD + tid] = __float2bfloat16_rn(p.scale * fmaf(qq, d, ww));
+            p.out[(tok * Ho + ho) * kD + tid] = __float2bfloat16_rn(p.scale * fmaf(qq, d, ww));
         }
         __syncthreads();
 
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_kernel(const Decode
         if (t + 1 < p.T) __syncthreads();
     }
 
-    if (p.sfin) {
+    if (p.sfin && hm.state_owner) {
         float* dst = static_cast<float*>(p.sfin) + soff;
 #pragma unroll
         for (int r = 0; r < kDecRows; ++r) state_store(dst + (size_t)r * kD, s[r]);
@@ -158,11 +158,12 @@ __global__ void __launch_bounds__(kDecB16Threads, 3) kda_decode_bf16_kernel(cons
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hw = lane >> 4, c0 = (lane & 15) * 8;
-    const int64_t nh = blockIdx.x;
-    const int64_t n = nh / p.H;
-    const int h = (int)(nh % p.H);
+    const int Ho = p.Hq > p.H ? p.Hq : p.H, Hk = p.Hq > p.H ? p.H : p.Hq;
+    const int64_t n = (int64_t)blockIdx.x / Ho;
+    const int ho = (int)(blockIdx.x % Ho);
+    const HeadMap hm = head_map(ho, p.H, p.Hq);
     const int rbase = warp * 32 + hw;  // this thread's rows: rbase + 2 i
-    const size_t soff = (size_t)nh * kD * kD + (size_t)rbase * kD + c0;
+    const size_t soff = ((size_t)n * p.H + hm.hs) * kD * kD + (size_t)rbase * kD + c0;
 
     uint4 s[kDecB16Rows];
     if (p.s0) {
@@ -175,14 +176,13 @@ __global__ void __launch_bounds__(kDecB16Threads, 3) kda_decode_bf16_kernel(cons
         for (int i = 0; i < kDecB16Rows; ++i) s[i] = make_uint4(0u, 0u, 0u, 0u);
     }
 
-    const size_t row0 = (size_t)n * p.T * p.H + h;
     for (int64_t t = 0; t < p.T; ++t) {
-        const size_t row = row0 + (size_t)t * p.H;
-        const size_t e = row * kD + tid;
-        s_k[tid] = __bfloat162float(p.k[e]);
-        s_q[tid] = __bfloat162float(p.q[e]);
-        s_v[tid] = __bfloat162float(p.v[e]);
-        s_e[tid] = expf(p.g[e]);
+        const size_t tok = (size_t)n * p.T + t;
+        const size_t row = tok * p.H + hm.hs;
+        s_k[tid] = __bfloat162float(p.k[(tok * Hk + hm.hk) * kD + tid]);
+        s_q[tid] = __bfloat162float(p.q[(tok * p.Hq + hm.hq) * kD + tid]);
+        s_v[tid] = __bfloat162float(p.v[row * kD + tid]);
+        s_e[tid] = expf(p.g[row * kD + tid]);
         const float beta_t = __bfloat162float(p.beta[row]);
         __syncthreads();
 
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kDecB16Threads, 3) kda_decode_bf16_kernel(cons
             }
             const float d = beta_t * (s_v[tid] - uu);
             s_d[tid] = d;
-            p.out[row * kD + tid] = __float2bfloat16_rn(p.scale * fmaf(qq, d, ww));
+            p.out[(tok * Ho + ho) * kD + tid] = __float2bfloat16_rn(p.scale * fmaf(qq, d, ww));
         }
         __syncthreads();
 
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kDecB16Threads, 3) kda_decode_bf16_kernel(cons
         if (t + 1 < p.T) __syncthreads();
     }
 
-    if (p.sfin) {
+    if (p.sfin && hm.state_owner) {
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.sfin) + soff;
 #pragma unroll
         for (int i = 0; i < kDecB16Rows; ++i)
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kDecB16Threads, 3) kda_decode_bf16_kernel(cons
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
-    const int64_t rows = (int64_t)p.N * p.H;
+    const int64_t rows = (int64_t)p.N * (p.Hq > p.H ? p.Hq : p.H);
     if (rows == 0) return cudaSuccess;
     const dim3 grid((unsigned)rows);
     if (p.state_bf16)

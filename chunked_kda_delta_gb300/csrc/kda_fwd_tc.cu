@@ -182,6 +182,9 @@ __device__ __forceinline__ void gram16(uint32_t abase, uint32_t bbase, int lane,
         for (int e = 0; e < 4; ++e) c[j][e] = acc[0][j][e] + acc[1][j][e];
 }
 
+// kGrouped: unequal head counts (HeadMap); the equal-count instance keeps the plain
+// head indexing, which leaves the state chain two registers it needs.
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -190,9 +193,11 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();   // 0: K1 CTA, 1: K2 CTA
-    const int unit = blockIdx.x >> 1;          // (row, head) of this cluster
-    const int h = unit % p.H;
-    const int n = unit / p.H;
+    // (row, output head) of this cluster; the roles below look up their other heads
+    const int Ho0 = kGrouped ? (p.Hq > p.H ? p.Hq : p.H) : p.H;
+    const int n = (int)((blockIdx.x >> 1) / Ho0);
+    const int h = kGrouped ? head_map((int)((blockIdx.x >> 1) % Ho0), p.H, p.Hq).hs
+                           : (int)((blockIdx.x >> 1) % Ho0);  // state head
     int64_t bos, eos;
     int seq_id, seg_id, seg_count;
     if (!seq_range(p, n, bos, eos, seq_id, seg_id, seg_count)) return;  // both CTAs return
@@ -274,8 +279,14 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (lane == 0) {
                 const int32_t t0 = (int32_t)(bos + (int64_t)c * kChunk);
                 mbar_arrive_expect_tx(bar(BAR_IN_FULL + s), kTxBytes);
-                tma_load_3d(dst + kInQ, &tm_q, bar(BAR_IN_FULL + s), 0, h, t0);
-                tma_load_3d(dst + kInK, &tm_k, bar(BAR_IN_FULL + s), 0, h, t0);
+                int hq = h, hk = h;
+                if (kGrouped) {
+                    const HeadMap hm = head_map((int)((blockIdx.x >> 1) % (p.Hq > p.H ? p.Hq : p.H)), p.H, p.Hq);
+                    hq = hm.hq;
+                    hk = hm.hk;
+                }
+                tma_load_3d(dst + kInQ, &tm_q, bar(BAR_IN_FULL + s), 0, hq, t0);
+                tma_load_3d(dst + kInK, &tm_k, bar(BAR_IN_FULL + s), 0, hk, t0);
                 tma_load_3d(dst + kInV, &tm_v, bar(BAR_IN_FULL + s), 0, h, t0);
                 tma_load_3d(dst + kInG, &tm_g, bar(BAR_IN_FULL + s), 0, h, t0);
             }
@@ -539,6 +550,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         //   warp 9      tells each K1 group when its bulk copy has landed.
         volatile int32_t* k2fail = reinterpret_cast<volatile int32_t*>(smem + kSmK2Fail);
         const bool with_out = (p.flags & kFlagNoOutput) == 0;
+        // Output heads and this cluster's output head, recomputed where used so that they
+        // hold no registers across the chunk loop.
+        auto out_heads = [&]() { return kGrouped ? (p.Hq > p.H ? p.Hq : p.H) : p.H; };
+        auto out_head = [&]() { return kGrouped ? (int)((blockIdx.x >> 1) % out_heads()) : h; };
         const uint32_t idesc32 = idesc_bf16(128, 32), idesc128 = idesc_bf16(128, 128),
                        idesc16 = idesc_bf16(128, 16);
         const uint32_t idesc1 = with_out ? idesc32 : idesc16;  // MMA1 N: W and Qtil, or W only
@@ -708,7 +723,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     // commits later, so the drain below (all but the two newest stores)
                     // covers the store of the chunk four back, whose tile comes next.
                     const int32_t t0p = (int32_t)(bos + (int64_t)(c - 1) * kChunk);
-                    tma_store_3d(&tm_out, sbase + kSmOTile + ((c - 1) % kOTiles) * kOTileBytes, 0, h, t0p);
+                    tma_store_3d(&tm_out, sbase + kSmOTile + ((c - 1) % kOTiles) * kOTileBytes, 0, out_head(), t0p);
                     bulk_commit();
                     bulk_wait_read<2>();
                 }
@@ -727,7 +742,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // runs) at sequence b for the last segment only.
             const size_t soff = ((size_t)n * p.H + h) * kD * kD;
             size_t foff = soff;
-            bool write_final = p.sfin != nullptr;
+            bool write_final = p.sfin != nullptr && (!kGrouped || head_map(out_head(), p.H, p.Hq).state_owner);
             if (p.flags & kFlagFinalLastSeg) {
                 write_final = write_final && seg_id == seg_count - 1;
                 foff = ((size_t)seq_id * p.H + h) * kD * kD;
@@ -789,7 +804,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                     for (int r = 0; r < 8; ++r) {
                         const int row = 8 * hf + r;
-                        if (row < Cp) p.out[((t0p + row) * H + h) * kD + j] = __float2bfloat16_rn(p.scale * o[r]);
+                        if (row < Cp)
+                            p.out[((t0p + row) * out_heads() + out_head()) * kD + j] =
+                                __float2bfloat16_rn(p.scale * o[r]);
                     }
                 }
             };
@@ -900,12 +917,13 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
 size_t serial_smem_bytes() { return kSmemBytes; }
 int serial_block_threads() { return kThreads; }
-const void* serial_kernel_symbol() { return reinterpret_cast<const void*>(&kda_fwd_tc_kernel); }
+const void* serial_kernel_symbol() { return reinterpret_cast<const void*>(&kda_fwd_tc_kernel<false>); }
+const void* grouped_kernel_symbol() { return reinterpret_cast<const void*>(&kda_fwd_tc_kernel<true>); }
 
 cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream_t stream) {
     const long long rows = p.seg_len > 0 ? (p.cu ? (long long)p.rows : (long long)p.N * p.nseg_used)
                                          : (long long)p.N;
-    const long long clusters = rows * p.H;
+    const long long clusters = rows * (p.Hq > p.H ? p.Hq : p.H);
     if (clusters == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
@@ -919,7 +937,11 @@ cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kda_fwd_tc_kernel, maps.q, maps.k, maps.v, maps.g, maps.out, p);
+    if (p.Hq != p.H)
+        return cudaLaunchKernelEx(&cfg, kda_fwd_tc_kernel<true>, maps.q, maps.k, maps.v, maps.g,
+                                  maps.out, p);
+    return cudaLaunchKernelEx(&cfg, kda_fwd_tc_kernel<false>, maps.q, maps.k, maps.v, maps.g,
+                              maps.out, p);
 }
 
 }  // namespace kda

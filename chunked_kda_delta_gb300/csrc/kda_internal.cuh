@@ -31,7 +31,8 @@ struct FwdParams {
     int64_t T_total;
     int64_t dense_len;    // tokens per sequence when cu == nullptr
     int32_t N;
-    int32_t H;
+    int32_t H;            // heads of v, g, beta and the states
+    int32_t Hq;           // heads of q (k has min(Hq, H), the output max(Hq, H))
     float scale;
     int64_t wait_limit;   // iteration limit of bounded spin waits
     int32_t debug_flags;  // KDA_DEBUG_* bits (failure-path tests only)
@@ -62,10 +63,36 @@ struct DecodeParams {
     __nv_bfloat16* out;       // [N][T][H][128]
     int64_t T;
     int32_t N;
-    int32_t H;
+    int32_t H;                // heads of v, g, beta and the states
+    int32_t Hq;               // heads of q; see HeadMap
     float scale;
     int32_t state_bf16;       // 1: states are bf16, else fp32
 };
+
+// Grouped heads.  H state heads (v, g, beta, states), Hq query heads, min(Hq, H) key
+// heads and Ho = max(Hq, H) output heads, one of the two a multiple of the other.
+// Output head ho reads q head hq, k head hk and state head hs:
+//   Hq <= H (grouped value heads): hs = ho, hq = hk = ho / (H / Hq);
+//   Hq >  H (grouped query heads):  hq = ho, hs = hk = ho / (Hq / H); the Hq / H output
+//           heads of a state head run the same chain, and the first writes its state.
+struct HeadMap {
+    int hq, hk, hs;
+    bool state_owner;
+};
+__host__ __device__ inline HeadMap head_map(int ho, int H, int Hq) {
+    HeadMap m;
+    if (Hq <= H) {
+        m.hs = ho;
+        m.hq = m.hk = ho / (H / Hq);
+        m.state_owner = true;
+    } else {
+        const int G = Hq / H;
+        m.hq = ho;
+        m.hs = m.hk = ho / G;
+        m.state_owner = (ho % G) == 0;
+    }
+    return m;
+}
 
 // Launch flags of the fused kernel.
 constexpr int32_t kFlagNoOutput = 1;       // no output rows (summary runs)
@@ -132,7 +159,8 @@ struct TensorMaps {
 };
 
 // Launchers (return the launch error, cudaSuccess on success).
-// Fused K1+K2 kernel over p.N x p.H rows (or the segment rows of a segment launch).
+// Fused K1+K2 kernel over p.N x max(p.Hq, p.H) rows (or the segment rows of a segment
+// launch, which need Hq == H).
 cudaError_t launch_serial(const FwdParams& p, const TensorMaps& maps, cudaStream_t stream);
 // Segment merge: carry[b][0] = S0[b] (or 0), carry[b][s+1] = m[b][s] carry[b][s] + bs[b][s].
 // Varlen segment table: seg_start[n] = sum over sequences before n of
@@ -148,7 +176,8 @@ cudaError_t launch_merge(const float* m_seg, const float* b_seg, const float* s0
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 size_t serial_smem_bytes();
 int serial_block_threads();
-const void* serial_kernel_symbol();
+const void* serial_kernel_symbol();   // equal head counts
+const void* grouped_kernel_symbol();  // grouped heads (same shared memory and block size)
 size_t merge_smem_bytes();
 const void* merge_kernel_symbol();
 

@@ -43,6 +43,19 @@ class Workload:
     seed: int
     head_dim: int = D_HEAD
     decode: bool = False     # True: one decode step (kda_decode) per sequence, not a prefill
+    num_q_heads: int = 0     # heads of q (0: num_heads); k has min(Hq, H), out max(Hq, H)
+
+    @property
+    def q_heads(self) -> int:
+        return self.num_q_heads or self.num_heads
+
+    @property
+    def k_heads(self) -> int:
+        return min(self.q_heads, self.num_heads)
+
+    @property
+    def out_heads(self) -> int:
+        return max(self.q_heads, self.num_heads)
 
     @property
     def total_tokens(self) -> int:
@@ -54,7 +67,8 @@ class Workload:
 
     @property
     def head_tokens(self) -> int:
-        return self.total_tokens * self.num_heads
+        """Tokens x output heads: the units of work of a step."""
+        return self.total_tokens * self.out_heads
 
 
 def varlen_h12_lengths(seed: int = 3) -> tuple:
@@ -76,15 +90,22 @@ WORKLOADS = {
     # one decode step of a batch of 256 sequences over 64 heads (a state cache of
     # 256 x 64 states: 1 GiB in fp32, larger than L2)
     "decode_b256_h64": Workload("decode_b256_h64", (1,) * 256, 64, True, True, 6, decode=True),
+    # grouped heads at the single-sequence size: 16 q/k heads shared by 64 state heads,
+    # and 64 query heads sharing 16 k/v/g/beta heads
+    "gva_t8192_q16_v64": Workload("gva_t8192_q16_v64", (8192,), 64, True, True, 7,
+                                  num_q_heads=16),
+    "gqa_t8192_q64_v16": Workload("gqa_t8192_q64_v16", (8192,), 16, True, True, 8,
+                                  num_q_heads=64),
 }
 
 
 def custom(seq_lens: Sequence[int], num_heads: int, has_initial_state: bool, seed: int,
-           dense: Optional[bool] = None, name: str = "custom") -> Workload:
+           dense: Optional[bool] = None, name: str = "custom", num_q_heads: int = 0) -> Workload:
     lens = tuple(int(x) for x in seq_lens)
     if dense is None:
         dense = len(set(lens)) == 1 and len(lens) >= 1 and lens[0] > 0
-    return Workload(name, lens, int(num_heads), bool(has_initial_state), bool(dense), int(seed))
+    return Workload(name, lens, int(num_heads), bool(has_initial_state), bool(dense), int(seed),
+                    num_q_heads=int(num_q_heads))
 
 
 def to_bf16_rne(x: torch.Tensor) -> torch.Tensor:
@@ -95,8 +116,9 @@ def to_bf16_rne(x: torch.Tensor) -> torch.Tensor:
 def make_inputs(w: Workload, device="cpu", stress: bool = False) -> dict:
     """Draw the inputs of workload ``w`` on ``device``.
 
-    Returns a dict with q, k, v (bf16 [T, H, D]), g (fp32 [T, H, D]),
-    beta (bf16 [T, H]), initial_state (fp32 [N, H, D, D] or None),
+    Returns a dict with q, k, v (bf16 [T, H, D]; with grouped heads q has Hq heads and
+    k min(Hq, H)), g (fp32 [T, H, D]), beta (bf16 [T, H]), initial_state (fp32 [N, H, D, D]
+    or None),
     cu_seqlens (int32 [N + 1] on ``device``; always present), seq_lens,
     scale (float) and the workload itself.
     """
@@ -113,8 +135,8 @@ def make_inputs(w: Workload, device="cpu", stress: bool = False) -> dict:
         n = torch.linalg.vector_norm(x, dim=-1, keepdim=True)
         return x / torch.clamp(n, min=1e-30)
 
-    q = to_bf16_rne(unit(randn(T, H, D)))
-    k = to_bf16_rne(unit(randn(T, H, D)))
+    q = to_bf16_rne(unit(randn(T, w.q_heads, D)))
+    k = to_bf16_rne(unit(randn(T, w.k_heads, D)))
     v = to_bf16_rne(randn(T, H, D))
     if stress:
         g = -torch.abs(randn(T, H, D) * 0.02)

@@ -8,6 +8,7 @@ compiled library is missing or the call fails, :class:`KdaError` is raised.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import threading
 from typing import Optional
@@ -49,7 +50,7 @@ class KdaError(RuntimeError):
 class KdaShape(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("seq_len", ctypes.c_int64),
                 ("num_seqs", ctypes.c_int32), ("num_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("num_q_heads", ctypes.c_int32)]
 
 
 class KdaOptions(ctypes.Structure):
@@ -121,18 +122,25 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _shape_of(q: torch.Tensor, cu_seqlens) -> KdaShape:
+def _shape_of(q: torch.Tensor, v: torch.Tensor, cu_seqlens) -> KdaShape:
+    """Shape of a call: batch and tokens from q, state heads from v, query heads from q."""
     if q.dim() == 4:
-        B, T, H, D = q.shape
+        B, T, Hq, D = q.shape
     elif q.dim() == 3:
-        B, (T, H, D) = 1, q.shape
+        B, (T, Hq, D) = 1, q.shape
     else:
         raise ValueError("q must be [T, H, 128] or [B, T, H, 128]")
+    H = v.shape[-2]
     if cu_seqlens is not None:
         if B != 1:
             raise ValueError("packed varlen input needs batch 1")
-        return KdaShape(1, T, cu_seqlens.numel() - 1, H, D)
-    return KdaShape(B, T, 0, H, D)
+        return KdaShape(1, T, cu_seqlens.numel() - 1, H, D, Hq)
+    return KdaShape(B, T, 0, H, D, Hq)
+
+
+def _out_shape(q: torch.Tensor, v: torch.Tensor):
+    """q's shape with max(query heads, state heads) heads."""
+    return tuple(q.shape[:-2]) + (max(q.shape[-2], v.shape[-2]), q.shape[-1])
 
 
 def _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, device_type):
@@ -145,10 +153,17 @@ def _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, device_type):
             raise ValueError(f"{name} must be contiguous")
         if t.device.type != device_type:
             raise ValueError(f"{name} must be on {device_type}")
-    if q.shape != k.shape or q.shape != v.shape or q.shape != g.shape:
-        raise ValueError("q, k, v, g must share one shape")
-    if beta.shape != q.shape[:-1]:
-        raise ValueError("beta must have q's shape without the last dim")
+    if v.shape != g.shape:
+        raise ValueError("v and g must share one shape")
+    if q.dim() != v.dim() or q.shape[:-2] != v.shape[:-2] or q.shape[-1] != v.shape[-1]:
+        raise ValueError("q and v must agree in every dim but heads")
+    Hq, H = q.shape[-2], v.shape[-2]
+    if Hq < 1 or H < 1 or (Hq % H and H % Hq):
+        raise ValueError(f"query heads ({Hq}) and state heads ({H}) must divide one another")
+    if k.shape != q.shape[:-2] + (min(Hq, H), q.shape[-1]):
+        raise ValueError("k must have min(query heads, state heads) heads")
+    if beta.shape != v.shape[:-1]:
+        raise ValueError("beta must have v's shape without the last dim")
     if initial_state is not None:
         if initial_state.dtype != torch.float32 or not initial_state.is_contiguous():
             raise ValueError("initial_state must be contiguous float32")
@@ -159,6 +174,17 @@ def _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, device_type):
             raise ValueError("cu_seqlens must be contiguous int32")
         if cu_seqlens.device.type != device_type:
             raise ValueError(f"cu_seqlens must be on {device_type}")
+
+
+def _check_result(name, t, shape, dtype, device_type):
+    """A caller-supplied output must be exactly what the library writes: the C ABI takes
+    bare pointers and cannot see a short buffer."""
+    if t is None:
+        return
+    if t.dtype != dtype or not t.is_contiguous() or t.device.type != device_type:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor on {device_type}")
+    if tuple(t.shape) != tuple(shape) and t.numel() != math.prod(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 DEBUG_STALL_WAIT = 1
@@ -181,7 +207,9 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
 
     q, k, v: bf16 ``[T, H, 128]`` (or ``[B, T, H, 128]`` dense); g: fp32 of the
     same shape; beta: bf16 ``[T, H]``; initial_state / final_state: fp32
-    ``[N, H, 128, 128]``; cu_seqlens: int32 ``[N + 1]`` on the device.  ``out``
+    ``[N, H, 128, 128]``; cu_seqlens: int32 ``[N + 1]`` on the device.  Grouped heads:
+    q may have Hq heads, Hq a multiple or a divisor of v's H (k then has min(Hq, H)
+    heads, the output max(Hq, H)).  ``out``
     is allocated when not given; ``final_state`` is allocated when
     ``output_final_state`` is set and none is given (pass ``final_state =
     initial_state`` to update in place).  The call is asynchronous on
@@ -189,12 +217,14 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
     """
     lib = load_library()
     _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, "cuda")
-    shape = _shape_of(q, cu_seqlens)
+    shape = _shape_of(q, v, cu_seqlens)
     N = shape.num_seqs if cu_seqlens is not None else shape.batch
     if scale is None:
         scale = shape.head_dim ** -0.5
+    _check_result("out", out, _out_shape(q, v), torch.bfloat16, "cuda")
+    _check_result("final_state", final_state, (N, shape.num_heads, 128, 128), torch.float32, "cuda")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(_out_shape(q, v), dtype=q.dtype, device=q.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, shape.num_heads, shape.head_dim, shape.head_dim),
                                   dtype=torch.float32, device=q.device)
@@ -227,12 +257,14 @@ def kda_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
     """
     lib = load_library()
     _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, "cpu")
-    shape = _shape_of(q, cu_seqlens)
+    shape = _shape_of(q, v, cu_seqlens)
     N = shape.num_seqs if cu_seqlens is not None else shape.batch
     if scale is None:
         scale = shape.head_dim ** -0.5
+    _check_result("out", out, _out_shape(q, v), torch.bfloat16, "cpu")
+    _check_result("final_state", final_state, (N, shape.num_heads, 128, 128), torch.float32, "cpu")
     if out is None:
-        out = torch.empty_like(q, pin_memory=q.is_pinned())
+        out = torch.empty(_out_shape(q, v), dtype=q.dtype, pin_memory=q.is_pinned())
     if final_state is None and output_final_state:
         final_state = torch.empty((N, shape.num_heads, shape.head_dim, shape.head_dim),
                                   dtype=torch.float32, pin_memory=q.is_pinned())
@@ -314,7 +346,10 @@ def kda_prefill_segment_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
     """
     lib = load_library()
     _check_tensors(q, k, v, g, beta, initial_state, None, "cuda")
-    shape = _shape_of(q, None)
+    shape = _shape_of(q, v, None)
+    _check_result("out", out, _out_shape(q, v), torch.bfloat16, "cuda")
+    _check_result("final_state", final_state, (shape.batch, shape.num_heads, 128, 128),
+                  torch.float32, "cuda")
     if scale is None:
         scale = shape.head_dim ** -0.5
     if stream is None:
@@ -339,7 +374,8 @@ def kda_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tenso
     """The recurrent decode step on CUDA tensors; returns ``(out, final_state)``.
 
     q, k, v: bf16 ``[B, H, 128]`` (one token per sequence) or ``[B, T, H, 128]``;
-    g: fp32 of the same shape; beta: bf16 ``[B, H]`` or ``[B, T, H]``.  States are
+    g: fp32 of v's shape; beta: bf16 ``[B, H]`` or ``[B, T, H]``; grouped heads as in
+    :func:`kda_prefill`.  States are
     ``[B, H, 128, 128]`` in fp32 or bf16 (``state_dtype``, else the dtype of the
     state tensors given, else fp32).  Pass ``final_state = initial_state`` to update a
     state cache in place; a new final state is allocated when ``output_final_state``
@@ -353,7 +389,8 @@ def kda_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tenso
     _check_tensors(q, k, v, g, beta, None, None, "cuda")
     if q.dim() != 4:
         raise ValueError("q must be [B, H, 128] or [B, T, H, 128]")
-    B, T, H, D = q.shape
+    B, T, Hq, D = q.shape
+    H = v.shape[2]
     given = [t for t in (initial_state, final_state) if t is not None]
     if state_dtype is None:
         state_dtype = given[0].dtype if given else torch.float32
@@ -366,15 +403,16 @@ def kda_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tenso
             raise ValueError(f"states must be [{B}, {H}, {D}, {D}]")
     if scale is None:
         scale = D ** -0.5
+    _check_result("out", out, _out_shape(q, v), torch.bfloat16, "cuda")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(_out_shape(q, v), dtype=q.dtype, device=q.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((B, H, D, D), dtype=state_dtype, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif isinstance(stream, torch.cuda.Stream):
         stream = stream.cuda_stream
-    shape = KdaShape(B, T, 0, H, D)
+    shape = KdaShape(B, T, 0, H, D, Hq)
     with torch.cuda.device(q.device):
         st = lib.kda_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                             ctypes.c_float(scale), _ptr(initial_state), _ptr(final_state),

@@ -22,7 +22,8 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- * Layouts (row-major, contiguous, C order):
+ * Layouts (row-major, contiguous, C order), H = num_heads (equal head counts; see
+ * kda_shape for grouped heads, where q, k and out have their own head counts):
  *   q, k, v, out : bf16 [T_total][H][128]   (dense input [B][T][H][128] is the same memory)
  *   g            : fp32 [T_total][H][128]   per-token log-decay (not cumulative)
  *   beta         : bf16 [T_total][H]
@@ -70,13 +71,26 @@ typedef enum kda_status {
 
 /* Problem shape.  Dense: cu_seqlens == NULL, `batch` sequences of `seq_len`
  * tokens each (T_total = batch * seq_len, N = batch).  Packed varlen:
- * cu_seqlens != NULL, batch == 1, seq_len = T_total, num_seqs = N >= 1. */
+ * cu_seqlens != NULL, batch == 1, seq_len = T_total, num_seqs = N >= 1.
+ *
+ * Grouped heads (the pages name GVA, unequal head counts, as a follow-up: cuLA PR #103,
+ * intracard-CP planner notes).  H = num_heads counts the heads of v, g, beta and the
+ * states; Hq = num_q_heads (0 means H) the heads of q; one must divide the other.  k has
+ * min(Hq, H) heads and out max(Hq, H):
+ *   Hq <= H  grouped value heads: state head h reads q and k head h / (H / Hq); the
+ *            output has a row per state head;
+ *   Hq >  H  grouped query heads: query head j reads k, v, g, beta and state head
+ *            j / (Hq / H); the output has a row per query head, and the state of a group
+ *            is written once.
+ * Grouped shapes run in serial mode (segment mode and kda_prefill_segment_noalloc reject
+ * them; KDA_MODE_AUTO picks serial). */
 typedef struct kda_shape {
     int32_t batch;
     int64_t seq_len;
-    int32_t num_seqs;   /* varlen only; ignored for dense input */
-    int32_t num_heads;  /* H >= 1; need not be a multiple of 8 */
-    int32_t head_dim;   /* must be 128 (Dk = Dv = 128) */
+    int32_t num_seqs;     /* varlen only; ignored for dense input */
+    int32_t num_heads;    /* H >= 1; need not be a multiple of 8 */
+    int32_t head_dim;     /* must be 128 (Dk = Dv = 128) */
+    int32_t num_q_heads;  /* heads of q; 0 = num_heads */
 } kda_shape;
 
 /* Execution modes of kda_prefill_ex. */

@@ -17,6 +17,8 @@ arrays.  Three forms of the same definition are exposed:
 * :func:`segmented` -- the segment pipeline "K1 once -> pre_scan -> merge ->
   segment-K2" (cuLA PR #103, "feat(kda/sm90): FlashKDA prefill port +
   intracard-CP prefill", commit notes).
+* :func:`grouped` -- any form over grouped (unequal) head counts, by running every
+  output head as a plain head on the tensors it reads.
 
 Every function takes float64 arrays: q, k, g ``[T, H, Dk]``; v ``[T, H, Dv]``;
 beta ``[T, H]``; optional ``s0`` ``[N, H, Dk, Dv]``; ``cu_seqlens`` (N+1
@@ -166,3 +168,42 @@ def segmented(*a, **kw):
 recurrent.__doc__ = OracleLib.recurrent.__doc__
 chunked.__doc__ = OracleLib.chunked.__doc__
 segmented.__doc__ = OracleLib.segmented.__doc__
+
+
+def grouped_heads(ho: int, H: int, Hq: int):
+    """(q head, k head, state head) read by output head ``ho`` when q has ``Hq`` heads and
+    v, g, beta and the states have ``H`` (one a multiple of the other; k has min(Hq, H)
+    heads, the output max(Hq, H)).  Unequal head counts are named as a follow-up in cuLA
+    PR #103 (intracard-CP planner notes: GVA); the two directions are read as: more
+    state heads than query heads shares each q/k head among H / Hq state heads; more query
+    heads than state heads shares each k/v/g/beta head, and its state, among Hq / H query
+    heads."""
+    if Hq <= H:
+        G = H // Hq
+        return ho // G, ho // G, ho
+    G = Hq // H
+    return ho, ho // G, ho // G
+
+
+def grouped(q, k, v, g, beta, scale, s0=None, cu_seqlens=None, form="recurrent", lib=None,
+            **kw):
+    """An oracle form over grouped heads: q ``[T, Hq, D]``, k ``[T, min(Hq, H), D]``, v and g
+    ``[T, H, D]``, beta ``[T, H]``, s0 ``[N, H, D, D]``.  Every output head is run as an
+    ungrouped head on the tensors it reads (:func:`grouped_heads`); returns
+    ``(out [T, max(Hq, H), Dv], final [N, H, Dk, Dv])``, the final state of a state head
+    taken from the first output head that reads it."""
+    lib = lib or default()
+    q, k, v, g, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
+    Hq, H = q.shape[1], v.shape[1]
+    if (Hq % H and H % Hq) or k.shape[1] != min(Hq, H) or g.shape != v.shape:
+        raise ValueError("head counts must divide one another; k has min(Hq, H) heads")
+    Ho = max(Hq, H)
+    maps = [grouped_heads(ho, H, Hq) for ho in range(Ho)]
+    iq = [m[0] for m in maps]
+    ik = [m[1] for m in maps]
+    isx = [m[2] for m in maps]
+    s0e = None if s0 is None else np.asarray(s0, dtype=np.float64)[:, isx]
+    out, fin = getattr(lib, form)(q[:, iq], k[:, ik], v[:, isx], g[:, isx], beta[:, isx], scale,
+                                  s0=s0e, cu_seqlens=cu_seqlens, **kw)
+    first = [isx.index(hs) for hs in range(H)]
+    return out, fin[:, first]

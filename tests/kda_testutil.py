@@ -13,6 +13,16 @@ ATOL = 1e-2
 RTOL = 1e-2
 
 
+def oracle_grouped(inp, form="recurrent", **kw):
+    """The oracle over an input dict with grouped heads (every output head); returns
+    (out [T, Ho, 128], final [N, H, 128, 128])."""
+    import oracle
+    f = lambda n: to_f64_numpy(inp[n])  # noqa: E731
+    cu = inp["cu_seqlens"].cpu().numpy().astype(np.int64)
+    return oracle.grouped(f("q"), f("k"), f("v"), f("g"), f("beta"), inp["scale"],
+                          s0=to_f64_numpy(inp["initial_state"]), cu_seqlens=cu, form=form, **kw)
+
+
 def oracle_on_heads(orc, inp, heads, form="recurrent", **kw):
     """Run the oracle on the given head indices of an input dict; returns (out, final)."""
     hs = list(heads)
@@ -54,3 +64,20 @@ def gpu_out_heads(out: torch.Tensor, heads):
 
 def gpu_state_heads(st: torch.Tensor, heads):
     return to_f64_numpy(st[:, list(heads)])
+
+
+def oracle_grouped_on_heads(orc, inp, out_heads, form="recurrent", **kw):
+    """The oracle on selected OUTPUT heads of a grouped input dict: each output head runs as
+    a plain head on the q, k and state heads it reads.  Returns (out [T, len, 128],
+    final [N, len, 128, 128]) where the final state is that of the head's state head."""
+    import oracle
+    w = inp["workload"]
+    maps = [oracle.grouped_heads(ho, w.num_heads, w.q_heads) for ho in out_heads]
+    sel = lambda n, idx: to_f64_numpy(inp[n][:, idx])  # noqa: E731
+    iq, ik, isx = ([m[i] for m in maps] for i in range(3))
+    s0 = inp["initial_state"]
+    cu = inp["cu_seqlens"].cpu().numpy().astype(np.int64)
+    return getattr(orc, form)(sel("q", iq), sel("k", ik), sel("v", isx), sel("g", isx),
+                              sel("beta", isx), inp["scale"],
+                              s0=None if s0 is None else to_f64_numpy(s0[:, isx]),
+                              cu_seqlens=cu, **kw)

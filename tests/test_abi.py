@@ -214,3 +214,39 @@ def test_decode_binding_checks_state_dtype():
     b = torch.zeros(2, 3, dtype=torch.bfloat16)
     with pytest.raises(ValueError):  # CPU tensors are refused before any library call
         K.kda_decode(q, q, q, g, b, initial_state=torch.zeros(2, 3, 128, 128))
+
+
+def test_grouped_head_rules(lib):
+    # num_q_heads must divide num_heads or be a multiple of it
+    assert _call(lib, KdaShape(1, 16, 0, 6, 128, 4)) == INVALID
+    assert _call(lib, KdaShape(1, 16, 0, 4, 128, -2)) == INVALID
+    assert _call(lib, KdaShape(1, 16, 0, 6, 128, 3)) not in (INVALID, ALIAS)
+    assert _call(lib, KdaShape(1, 16, 0, 2, 128, 8)) not in (INVALID, ALIAS)
+    # segment mode runs equal head counts only
+    assert _call(lib, KdaShape(1, 16, 0, 2, 128, 8), opts=KdaOptions(1, 64, 0, 0, 0)) == INVALID
+    # sizes follow the head counts: q of 8 heads is 32 KiB at T = 16
+    assert _call(lib, KdaShape(1, 16, 0, 2, 128, 8), out=0x10000000 + 16 * 1024) == ALIAS
+    assert _call(lib, KdaShape(1, 16, 0, 2, 128, 8), out=0x10000000 + 32 * 1024) not in (INVALID, ALIAS)
+    # the output has max(Hq, H) heads
+    assert _call(lib, KdaShape(1, 16, 0, 8, 128, 2), out=0x60000000,
+                 v=0x60000000 + 16 * 8 * 256 - 16) == ALIAS
+
+
+def test_grouped_planner_stays_serial(lib):
+    shape = KdaShape(1, 131072, 0, 4, 128, 2)
+    mode, seg = ctypes.c_int32(9), ctypes.c_int32(9)
+    assert lib.kda_plan(ctypes.byref(shape), 0, 76, ctypes.byref(mode), ctypes.byref(seg)) == 0
+    assert (mode.value, seg.value) == (K.MODE_SERIAL, 0)
+
+
+def test_binding_refuses_short_outputs():
+    # a caller-supplied output smaller than what the library writes is refused before the
+    # call (the ABI sees only a pointer); here q has 2 heads and v 6, so out has 6
+    q = torch.zeros(16, 2, 128, dtype=torch.bfloat16)
+    v = torch.zeros(16, 6, 128, dtype=torch.bfloat16)
+    g = torch.zeros(16, 6, 128, dtype=torch.float32)
+    b = torch.zeros(16, 6, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        K.kda_prefill_host(q, q, v, g, b, out=torch.zeros(16, 2, 128, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        K.kda_prefill_host(q, q, v, g, b, final_state=torch.zeros(1, 2, 128, 128))

@@ -369,3 +369,42 @@ def test_planted_mistakes_are_caught(tmp_path, name):
     mut = oracle.OracleLib(so)
     res = all_pins(mut)
     assert not all(res.values()), f"mutant {name} survived every pin: {res}"
+
+
+@pytest.mark.parametrize("Hq,H", [(2, 6), (6, 2), (3, 3), (1, 4), (4, 1)])
+def test_grouped_heads_single_token_closed_form(Hq, H):
+    """One token from the zero state: o = scale beta (q . k) v and S = beta k v^T, with
+    each output head reading the q, k and state heads the grouping assigns.  Distinct
+    values per head make a wrong head map (h * G for h / G, q and k swapped, the state
+    of the wrong group member) fail."""
+    rng = np.random.default_rng(40 + 7 * Hq + H)
+    D = 8
+    Hk, Ho = min(Hq, H), max(Hq, H)
+    q = rng.standard_normal((1, Hq, D))
+    k = rng.standard_normal((1, Hk, D))
+    v = rng.standard_normal((1, H, D))
+    g = -np.abs(rng.standard_normal((1, H, D)))
+    beta = rng.uniform(0.1, 1.0, (1, H))
+    scale = 0.37
+    out, fin = oracle.grouped(q, k, v, g, beta, scale)
+    assert out.shape == (1, Ho, D) and fin.shape == (1, H, D, D)
+    for ho in range(Ho):
+        if Hq <= H:
+            hq = hk = ho // (H // Hq)
+            hs = ho
+        else:
+            hq, hk, hs = ho, ho // (Hq // H), ho // (Hq // H)
+        want = scale * beta[0, hs] * np.dot(q[0, hq], k[0, hk]) * v[0, hs]
+        np.testing.assert_allclose(out[0, ho], want, rtol=1e-12, atol=1e-12)
+    for hs in range(H):
+        kk = k[0, hs // (H // Hq)] if Hq <= H else k[0, hs]
+        np.testing.assert_allclose(fin[0, hs], beta[0, hs] * np.outer(kk, v[0, hs]),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_grouped_heads_equal_counts_is_the_plain_oracle():
+    rng = np.random.default_rng(41)
+    q, k, v, g, beta, s0, cu = rand_problem(rng, [5, 0, 9], 3, 8, 8)
+    a = oracle.grouped(q, k, v, g, beta, 0.3, s0=s0, cu_seqlens=cu)
+    b = oracle.recurrent(q, k, v, g, beta, 0.3, s0=s0, cu_seqlens=cu)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
