@@ -303,9 +303,6 @@ kda_status validate_options(const kda_options* o, const Problem& pr, int32_t* mo
                     "segment_len must be a non-negative multiple of 16 (got %d)", o->segment_len);
     if (o->wait_limit < 0)
         return fail(KDA_ERR_INVALID_ARGUMENT, "wait_limit must be >= 0");
-    if (o->mode == KDA_MODE_SEGMENT && pr.Hq != pr.H)
-        return fail(KDA_ERR_INVALID_ARGUMENT,
-                    "segment mode needs num_q_heads == num_heads (grouped heads run serially)");
     *mode = o->mode;
     if (o->segment_len) *seg_len = o->segment_len;
     if (o->wait_limit) *wait_limit = o->wait_limit;
@@ -380,12 +377,14 @@ constexpr size_t kPlanWorkspaceCap = (size_t)4 << 30;
 void choose_plan(const Problem& pr, int64_t resident, int32_t* mode, int32_t* seg_len) {
     *mode = KDA_MODE_SERIAL;
     *seg_len = 0;
-    if (pr.varlen || pr.dense_len <= 0 || pr.Hq != pr.H) return;
-    const int64_t C = (int64_t)pr.N * pr.H;
+    if (pr.varlen || pr.dense_len <= 0) return;
+    // Chains of the summary passes (one per state head) and of the output pass (one per
+    // output head; more with grouped query heads).
+    const int64_t C = (int64_t)pr.N * pr.H, Co = (int64_t)pr.N * pr.Ho;
     const int64_t R = resident > 0 ? resident : 1;
     auto cdiv = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
     const int64_t nck = cdiv(pr.dense_len, kda::kChunk);
-    const double serial = (double)cdiv(C, R) * (double)nck;
+    const double serial = (double)cdiv(Co, R) * (double)nck;
     double best = serial;
     int32_t best_len = 0;
     for (int64_t sl = 512; sl <= ((int64_t)1 << 20); sl *= 2) {
@@ -393,7 +392,7 @@ void choose_plan(const Problem& pr, int64_t resident, int32_t* mode, int32_t* se
         if (nseg < 2) break;
         const size_t ws = (size_t)(3 * nseg - 2) * (size_t)C * kda::kD * kda::kD * 4;
         if (ws > kPlanWorkspaceCap) continue;
-        const double waves = (double)(2 * cdiv(C * (nseg - 1), R) + cdiv(C * nseg, R));
+        const double waves = (double)(2 * cdiv(C * (nseg - 1), R) + cdiv(Co * nseg, R));
         const double cost = waves * (double)(sl / kda::kChunk) + kMergePerSegment * (double)nseg;
         if (cost < best) {
             best = cost;
@@ -405,6 +404,11 @@ void choose_plan(const Problem& pr, int64_t resident, int32_t* mode, int32_t* se
         *seg_len = best_len;
     }
 }
+
+// Query heads a segment summary pass is launched with: summaries and transitions write
+// no output, so one cluster per state head does (with grouped query heads, the equal-count
+// instance, whose state head h reads k head h and an unused q head).
+int32_t summary_q_heads(const Problem& pr) { return pr.Hq > pr.H ? pr.H : pr.Hq; }
 
 // Varlen segment plan: sequence n gets max(1, ceil(len_n / seg_len)) segments, at most
 // N + floor(T_total / seg_len) in all; the table, summaries, transitions and carries are
@@ -487,7 +491,7 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
     if (mode == KDA_MODE_SEGMENT && pr.varlen) {
         const VarSegPlan vp = plan_segments_varlen(pr, seg_len);
         if (vp.rows > 0) {
-            if (vp.rows * 2 * pr.H > 0x7fffffffll)
+            if (vp.rows * 2 * pr.Ho > 0x7fffffffll)
                 return fail(KDA_ERR_INVALID_ARGUMENT, "too many segments for one launch");
             // Varlen segments: table -> pre_scan (summaries from zero, transitions from the
             // identity; every segment but each sequence's last) -> merge -> segment-K2.
@@ -502,6 +506,7 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
                                                stream)) != cudaSuccess)
                 return cuda_fail(e, "segment table launch");
             kda::FwdParams ps = p;
+            ps.Hq = summary_q_heads(pr);
             ps.seg_len = seg_len;
             ps.seg_start = table;
             ps.rows = (int32_t)vp.rows;
@@ -542,6 +547,7 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
     float* m_seg = reinterpret_cast<float*>(static_cast<char*>(ws) + sp.off_m);
     float* carries = reinterpret_cast<float*>(static_cast<char*>(ws) + sp.off_c);
     kda::FwdParams ps = p;
+    ps.Hq = summary_q_heads(pr);
     ps.seg_len = seg_len;
     ps.nseg_total = sp.nseg;
     ps.nseg_used = sp.nseg - 1;
@@ -862,9 +868,6 @@ extern "C" kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const 
     Problem pr{};
     kda_status st = validate_shape(shape, false, &pr);
     if (st != KDA_OK) return st;
-    if (pr.Hq != pr.H)
-        return fail(KDA_ERR_INVALID_ARGUMENT,
-                    "segment mode needs num_q_heads == num_heads (grouped heads run serially)");
     if (segment_len <= 0 || segment_len % kda::kChunk != 0)
         return fail(KDA_ERR_INVALID_ARGUMENT,
                     "segment_len must be a positive multiple of 16 (got %d)", segment_len);
@@ -925,6 +928,7 @@ extern "C" kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const 
     float* m_seg = reinterpret_cast<float*>(static_cast<char*>(scratch) + sp.off_m);
     float* carries = reinterpret_cast<float*>(static_cast<char*>(scratch) + sp.off_c);
     kda::FwdParams ps = p;
+    ps.Hq = summary_q_heads(pr);
     ps.seg_len = segment_len;
     ps.nseg_total = sp.nseg;
     ps.nseg_used = sp.nseg - 1;

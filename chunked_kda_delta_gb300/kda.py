@@ -285,11 +285,12 @@ def kda_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
 
 
 def kda_workspace_bytes(batch: int, seq_len: int, num_heads: int, mode: int = MODE_SERIAL,
-                        segment_len: int = 0, head_dim: int = 128, num_seqs: int = 0) -> int:
+                        segment_len: int = 0, head_dim: int = 128, num_seqs: int = 0,
+                        num_q_heads: int = 0) -> int:
     """Device workspace bytes for a problem of this shape in this mode (packed varlen
     when ``num_seqs`` > 0: ``batch`` 1, ``seq_len`` the total tokens)."""
     lib = load_library()
-    shape = KdaShape(batch, seq_len, num_seqs, num_heads, head_dim)
+    shape = KdaShape(batch, seq_len, num_seqs, num_heads, head_dim, num_q_heads)
     opts = _options(mode, segment_len, 0)
     n = ctypes.c_size_t(0)
     _check(lib, lib.kda_workspace_bytes(ctypes.byref(shape), ctypes.byref(opts),
@@ -298,11 +299,11 @@ def kda_workspace_bytes(batch: int, seq_len: int, num_heads: int, mode: int = MO
 
 
 def kda_plan(batch: int, seq_len: int, num_heads: int, resident_clusters: int,
-             varlen: bool = False, num_seqs: int = 0, head_dim: int = 128):
+             varlen: bool = False, num_seqs: int = 0, head_dim: int = 128, num_q_heads: int = 0):
     """The (mode, segment_len) that ``MODE_AUTO`` picks for this shape on a device holding
     ``resident_clusters`` co-resident clusters.  Host only."""
     lib = load_library()
-    shape = KdaShape(batch, seq_len, num_seqs, num_heads, head_dim)
+    shape = KdaShape(batch, seq_len, num_seqs, num_heads, head_dim, num_q_heads)
     mode, seg = ctypes.c_int32(0), ctypes.c_int32(0)
     _check(lib, lib.kda_plan(ctypes.byref(shape), int(bool(varlen)), int(resident_clusters),
                              ctypes.byref(mode), ctypes.byref(seg)))

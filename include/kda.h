@@ -82,8 +82,7 @@ typedef enum kda_status {
  *   Hq >  H  grouped query heads: query head j reads k, v, g, beta and state head
  *            j / (Hq / H); the output has a row per query head, and the state of a group
  *            is written once.
- * Grouped shapes run in serial mode (segment mode and kda_prefill_segment_noalloc reject
- * them; KDA_MODE_AUTO picks serial). */
+ * Every mode takes grouped shapes; segment summaries run once per state head. */
 typedef struct kda_shape {
     int32_t batch;
     int64_t seq_len;

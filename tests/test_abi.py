@@ -222,8 +222,8 @@ def test_grouped_head_rules(lib):
     assert _call(lib, KdaShape(1, 16, 0, 4, 128, -2)) == INVALID
     assert _call(lib, KdaShape(1, 16, 0, 6, 128, 3)) not in (INVALID, ALIAS)
     assert _call(lib, KdaShape(1, 16, 0, 2, 128, 8)) not in (INVALID, ALIAS)
-    # segment mode runs equal head counts only
-    assert _call(lib, KdaShape(1, 16, 0, 2, 128, 8), opts=KdaOptions(1, 64, 0, 0, 0)) == INVALID
+    # segment mode takes grouped heads too
+    assert _call(lib, KdaShape(1, 16, 0, 2, 128, 8), opts=KdaOptions(1, 64, 0, 0, 0)) not in (INVALID, ALIAS)
     # sizes follow the head counts: q of 8 heads is 32 KiB at T = 16
     assert _call(lib, KdaShape(1, 16, 0, 2, 128, 8), out=0x10000000 + 16 * 1024) == ALIAS
     assert _call(lib, KdaShape(1, 16, 0, 2, 128, 8), out=0x10000000 + 32 * 1024) not in (INVALID, ALIAS)
@@ -232,11 +232,18 @@ def test_grouped_head_rules(lib):
                  v=0x60000000 + 16 * 8 * 256 - 16) == ALIAS
 
 
-def test_grouped_planner_stays_serial(lib):
-    shape = KdaShape(1, 131072, 0, 4, 128, 2)
-    mode, seg = ctypes.c_int32(9), ctypes.c_int32(9)
-    assert lib.kda_plan(ctypes.byref(shape), 0, 76, ctypes.byref(mode), ctypes.byref(seg)) == 0
-    assert (mode.value, seg.value) == (K.MODE_SERIAL, 0)
+def test_grouped_planner(lib):
+    """Summary passes run one chain per state head, the output pass one per output head:
+    grouped value heads plan like their state heads; grouped query heads see cheaper
+    summaries than equal heads of the same output count."""
+    R = 76
+    assert K.kda_plan(1, 131072, 4, R, num_q_heads=2) == K.kda_plan(1, 131072, 4, R)
+    m, s = K.kda_plan(1, 131072, 2, R, num_q_heads=8)
+    assert m == K.MODE_SEGMENT and s % 16 == 0
+    assert K.kda_plan(1, 131072, 64, R, num_q_heads=16) == (K.MODE_SERIAL, 0)
+    # workspace: three state tables per (segment, state head)
+    nb = K.kda_workspace_bytes(1, 4096, 2, mode=K.MODE_SEGMENT, segment_len=1024, num_q_heads=8)
+    assert nb == (3 * 4 - 2) * 2 * 128 * 128 * 4
 
 
 def test_binding_refuses_short_outputs():

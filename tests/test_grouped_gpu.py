@@ -94,11 +94,39 @@ def test_auto_mode_runs_grouped_serially(orc):
     assert_close(to_f64_numpy(fin), f_ref, "auto final")
 
 
-def test_segment_mode_rejects_grouped_heads():
-    inp = make_inputs(custom([64], 4, False, seed=640, num_q_heads=2), DEV)
+@pytest.mark.parametrize("Hq,H", [(2, 6), (6, 2)])
+def test_segment_mode_grouped_dense(orc, Hq, H):
+    """Summaries and transitions run once per state head, the output pass once per output
+    head; slow decay so the carries matter."""
+    inp = make_inputs(custom([300, 300], H, True, seed=640 + Hq, num_q_heads=Hq), DEV,
+                      stress=True)
+    out, fin = run(inp, mode=K.MODE_SEGMENT, segment_len=64)
+    o_ref, f_ref = oracle_grouped(inp)
+    assert_close(to_f64_numpy(out), o_ref, "grouped segment out")
+    assert_close(to_f64_numpy(fin), f_ref, "grouped segment final")
+
+
+@pytest.mark.parametrize("Hq,H", [(3, 12), (12, 3)])
+def test_segment_mode_grouped_varlen(orc, Hq, H):
+    inp = make_inputs(custom([200, 3, 0, 97, 150], H, True, seed=645 + Hq, dense=False,
+                             num_q_heads=Hq), DEV, stress=True)
+    out, fin = run(inp, mode=K.MODE_SEGMENT, segment_len=48)
+    o_ref, f_ref = oracle_grouped(inp)
+    assert_close(to_f64_numpy(out), o_ref, "grouped varlen segment out")
+    assert_close(to_f64_numpy(fin), f_ref, "grouped varlen segment final")
+
+
+def test_segment_noalloc_grouped(orc):
+    inp = make_inputs(custom([256], 2, True, seed=648, num_q_heads=8), DEV, stress=True)
     x, _ = args_of(inp)
-    with pytest.raises(K.KdaError):
-        K.kda_prefill(**x, mode=K.MODE_SEGMENT, segment_len=32)
+    out = torch.empty(1, 256, 8, 128, dtype=torch.bfloat16, device=DEV)
+    fin = torch.empty(1, 2, 128, 128, device=DEV)
+    K.kda.kda_prefill_segment_noalloc(**x, out=out, segment_len=64, scale=inp["scale"],
+                                      initial_state=inp["initial_state"], final_state=fin)
+    torch.cuda.synchronize()
+    o_ref, f_ref = oracle_grouped(inp)
+    assert_close(to_f64_numpy(out.reshape(-1, 8, 128)), o_ref, "noalloc grouped out")
+    assert_close(to_f64_numpy(fin), f_ref, "noalloc grouped final")
 
 
 def test_host_entry_point_grouped():
