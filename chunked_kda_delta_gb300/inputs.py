@@ -98,6 +98,21 @@ WORKLOADS = {
                                   num_q_heads=64),
 }
 
+# The six H = 12 shapes timed on GB300 in flashinfer PR #4351 ("fix(cake_kda): support
+# non-aligned recurrent prefill head counts", Performance table): packed and mixed lists
+# are packed varlen batches, fixed shapes single dense sequences; no initial state, final
+# state returned (the PR's correctness runs compare output and complete final state).
+PAGES_H12 = {
+    "h12_packed_512x32": (512,) * 32,
+    "h12_packed_128x8": (128,) * 8,
+    "h12_fixed_512": (512,),
+    "h12_fixed_8192": (8192,),
+    "h12_mixed6": (1300, 547, 2048, 963, 271, 3063),
+    "h12_uniform_1024x8": (1024,) * 8,
+}
+for _i, (_name, _lens) in enumerate(PAGES_H12.items()):
+    WORKLOADS[_name] = Workload(_name, _lens, 12, False, len(_lens) == 1, 20 + _i)
+
 
 def custom(seq_lens: Sequence[int], num_heads: int, has_initial_state: bool, seed: int,
            dense: Optional[bool] = None, name: str = "custom", num_q_heads: int = 0) -> Workload:
