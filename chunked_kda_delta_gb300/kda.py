@@ -336,7 +336,8 @@ def kda_prefill_segment_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
                                 segment_len: int, scale: Optional[float] = None,
                                 initial_state: Optional[torch.Tensor] = None,
                                 final_state: Optional[torch.Tensor] = None, stream=None):
-    """Segment-parallel prefill with no device allocation (dense input only).
+    """Segment-parallel prefill with no device allocation (dense input only; grouped heads
+    allowed).
 
     For callers that cannot allocate device memory: the library keeps the segment
     scratch in a fixed 32 MiB device array shared by all calls, so ``out`` (and
