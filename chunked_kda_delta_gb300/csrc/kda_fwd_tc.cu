@@ -120,7 +120,8 @@ constexpr int kSmFail = kSmTmemSlot + 8;            // int32 per K1 group: failu
 constexpr int kSmK2Fail = kSmFail + 4 * kK1Groups;  // int32: K2 CTA failure flag
 constexpr int kSmLanded = kSmK2Fail + 4;            // int32: K2 CTA, chunks landed so far
 constexpr int kSmPrReady = kSmLanded + 4;           // int32: K2 CTA, [P ; R] operands written
-constexpr int kSmemBytes = kSmPrReady + 4;
+constexpr int kSmPrUsed = kSmPrReady + 4;           // int32: K2 CTA, [P ; R] operands consumed
+constexpr int kSmemBytes = kSmPrUsed + 4;
 static_assert(kSmPR + kPRSlots * kPRBytes <= kSmBar, "K2 buffers overlap the barriers");
 static_assert(kSmOTile % 128 == 0, "TMA store source must be 128-byte aligned");
 enum {  // K1 CTA barriers
@@ -227,6 +228,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             *reinterpret_cast<volatile int32_t*>(smem + kSmK2Fail) = 0;
             *reinterpret_cast<volatile int32_t*>(smem + kSmLanded) = 0;
             *reinterpret_cast<volatile int32_t*>(smem + kSmPrReady) = 0;
+            *reinterpret_cast<volatile int32_t*>(smem + kSmPrUsed) = 0;
             mbar_init(bar(BAR_NEVER), 1);
             for (int s = 0; s < kPRSlots; ++s) {
                 mbar_init(bar(BAR_PR_FULL + s), 1);
@@ -515,7 +517,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             fence_proxy_async_smem();
             named_bar_sync(nbar, 128);
-            if (kt == 0) {
+            // A thread of the group's last warp ships the chunk while thread 0 already
+            // waits for the next chunk's input tiles.
+            if (kt == 96) {
                 // Ship the chunk's operands into the K2 CTA's receive stage.
                 const int os = c % kRecvStages;
                 bool free_ok = c < kRecvStages ||
@@ -566,6 +570,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // wait, and otherwise falls back to it.
         int32_t* landed = reinterpret_cast<int32_t*>(smem + kSmLanded);
         int32_t* pr_ready = reinterpret_cast<int32_t*>(smem + kSmPrReady);
+        int32_t* pr_used = reinterpret_cast<int32_t*>(smem + kSmPrUsed);
         auto landed_or_wait = [&](int c) { return ld_acquire_cta(landed) > c || k1_full(c); };
         if ((p.debug_flags & 1) && !mbar_wait(bar(BAR_NEVER), 0, lim)) *k2fail = 1;  // never signalled
 
@@ -588,8 +593,13 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int m = 0; m + 1 < nchunks; ++m) {
                 const int slot = m % kPRSlots;
                 bool w = !*k2fail;
-                if (w && m >= kPRSlots) w = mbar_wait(bar(BAR_PR_FREE + slot), ((m / kPRSlots) - 1) & 1, lim);
-                w = w && k1_full(m) && k1_full(m + 1);
+                // Satisfied barrier waits cost this warp ~200 cycles each, and it works on
+                // every chunk: the progress counters answer first (operands m - 3 read by
+                // MMA1; chunks m and m + 1 landed), the barriers only when they lag.
+                if (w && m >= kPRSlots)
+                    w = ld_acquire_cta(pr_used) >= m - 2 ||
+                        mbar_wait(bar(BAR_PR_FREE + slot), ((m / kPRSlots) - 1) & 1, lim);
+                w = w && (ld_acquire_cta(landed) > m + 1 || (k1_full(m) && k1_full(m + 1)));
                 if (__any_sync(0xffffffffu, !w)) {
                     if (lane == 0) record(p.status, kStatusTimeout);
                     break;
@@ -848,7 +858,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (w) {
                         tc_fence_after();
                         // MMA1(c) has read D_c and [P_{c-1} ; R_{c-1}]: overwrite / hand back.
-                        if (warp == 8 && lane == 0 && c > 0) mbar_arrive(bar(BAR_PR_FREE + (c - 1) % kPRSlots));
+                        if (warp == 8 && lane == 0 && c > 0) {
+                            mbar_arrive(bar(BAR_PR_FREE + (c - 1) % kPRSlots));
+                            st_release_cta(pr_used, c);  // operands 0 .. c-1 read
+                        }
                         if (has_next) tmem_st32(tSA, pk);
                         // delta^T = U^T - (W D + P delta_prev)^T for rows 8hf .. 8hf+7
                         float dsum[8];
