@@ -213,10 +213,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     if (tid == 0) {
         if (rank == 0) {
-            // IN_FULL: the tiles' transaction bytes plus two arrivals (the TMA issue and
-            // the beta rows, written once their plain loads return).
             for (int s = 0; s < kInStages; ++s) {
-                mbar_init(bar(BAR_IN_FULL + s), 2);
+                mbar_init(bar(BAR_IN_FULL + s), 1);
                 mbar_init(bar(BAR_IN_EMPTY + s), 1);
             }
             for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_OUT_FREE + s), 1);
@@ -243,32 +241,11 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
-    // Input tiles of chunk c into ring stage c % kInStages (the producer thread only).
-    auto issue_tiles = [&](int c) {
-        const int s = c % kInStages;
-        const uint32_t dst = sbase + kSmIn + s * kInBytes;
-        const int32_t t0 = (int32_t)(bos + (int64_t)c * kChunk);
-        int hq = h, hk = h;
-        if (kGrouped) {
-            const HeadMap hm = head_map((int)((blockIdx.x >> 1) % (p.Hq > p.H ? p.Hq : p.H)), p.H, p.Hq);
-            hq = hm.hq;
-            hk = hm.hk;
-        }
-        mbar_arrive_expect_tx(bar(BAR_IN_FULL + s), kTxBytes);
-        tma_load_3d(dst + kInQ, &tm_q, bar(BAR_IN_FULL + s), 0, hq, t0);
-        tma_load_3d(dst + kInK, &tm_k, bar(BAR_IN_FULL + s), 0, hk, t0);
-        tma_load_3d(dst + kInV, &tm_v, bar(BAR_IN_FULL + s), 0, h, t0);
-        tma_load_3d(dst + kInG, &tm_g, bar(BAR_IN_FULL + s), 0, h, t0);
-    };
-    // The first ring's tiles go out right after this thread initialised the barriers: they
-    // touch only this CTA's shared memory, so they need not wait for the cluster barrier.
-    const int preissued = nchunks < kInStages ? nchunks : kInStages;
-    if (rank == 0 && tid == 0 && nchunks > 0) {
+    if (rank == 0 && warp == 0 && lane == 0 && nchunks > 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_g);
-        for (int c = 0; c < preissued; ++c) issue_tiles(c);
     }
     tc_fence_before();
     cluster_sync();  // barriers of both CTAs initialised before any remote access
@@ -286,7 +263,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             return t < eos ? __bfloat162float(p.beta[t * H + h]) : 0.f;
         };
         float b_cur = load_beta(0), b_next = load_beta(1);
-        int issued = preissued;
+        int issued = 0;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % kInStages;
             const bool ok = c < kInStages ||
@@ -295,18 +272,27 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (lane == 0) record(p.status, kStatusTimeout);
                 break;
             }
-            // The tiles first (the first ring went out before the cluster barrier), then
-            // the beta rows, whose loads may still be in flight, and the second arrival.
-            if (c >= preissued) {
-                if (lane == 0) issue_tiles(c);
-                issued = c + 1;
-            }
+            const uint32_t dst = sbase + kSmIn + s * kInBytes;
             if (lane < kChunk)
                 reinterpret_cast<float*>(smem + kSmIn + s * kInBytes + kInBeta)[lane] = b_cur;
             b_cur = b_next;
             b_next = load_beta(c + 2);
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_IN_FULL + s));
+            if (lane == 0) {
+                const int32_t t0 = (int32_t)(bos + (int64_t)c * kChunk);
+                mbar_arrive_expect_tx(bar(BAR_IN_FULL + s), kTxBytes);
+                int hq = h, hk = h;
+                if (kGrouped) {
+                    const HeadMap hm = head_map((int)((blockIdx.x >> 1) % (p.Hq > p.H ? p.Hq : p.H)), p.H, p.Hq);
+                    hq = hm.hq;
+                    hk = hm.hk;
+                }
+                tma_load_3d(dst + kInQ, &tm_q, bar(BAR_IN_FULL + s), 0, hq, t0);
+                tma_load_3d(dst + kInK, &tm_k, bar(BAR_IN_FULL + s), 0, hk, t0);
+                tma_load_3d(dst + kInV, &tm_v, bar(BAR_IN_FULL + s), 0, h, t0);
+                tma_load_3d(dst + kInG, &tm_g, bar(BAR_IN_FULL + s), 0, h, t0);
+            }
+            issued = c + 1;
         }
         // Drain: every issued load must have landed before the CTA exits.
         if (lane == 0)
