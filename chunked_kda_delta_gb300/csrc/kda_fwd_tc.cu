@@ -38,7 +38,7 @@
 //     shared::cluster copy that completes the K2 CTA's barrier.
 //   CTA rank 1 ("K2 CTA"): warps 1-8 run the state chain (decay and bf16 copy of the
 //     state, delta, output rows) and only arrive on two named barriers; warp 11 issues
-//     the state update, warps 12 and 0 the Mq term and MMA1 of the next chunk (the
+//     the state update and the Mq term, warps 12 and 0 MMA1 of the next chunk (the
 //     tensor pipe runs one thread's MMAs in order but overlaps different threads'), warp
 //     0 also owns TMEM and issues the output tiles' TMA stores; warp 10 computes
 //     [P ; R] ahead of the chain; warp 9 relays copy landings back to the K1 groups and
@@ -666,6 +666,11 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (live)
                         mma_ts(tmem + kColS, tmem + kColDA + 8u * (c & 1), sdesc(stage(c) + kB2, kLbo, kSboB2),
                                idesc128, 1);
+                    // Mq_c delta_c into chunk c's output partial (MMA1(c) wrote it; the chain
+                    // reads it after this commit), kept off the MMA1 issuers' path.
+                    if (live && with_out)
+                        mma_ts(tmem + kColD1 + kD1Buf * (c & 1) + 16, tmem + kColDA + 8u * (c & 1),
+                               sdesc(stage(c) + kB3, kLbo, kSboB3), idesc16, 1);
                     tc_commit(bar(BAR_SDONE));
                 }
                 __syncwarp();
@@ -675,10 +680,11 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     mbar_arrive_remote_relaxed(mapa(bar(BAR_OUT_FREE + (c - 1) % kRecvStages), 0));
             }
         } else if (warp == 12 || warp == 0) {
-            // ---- after EMIT(c): warp 12 issues Mq_c delta_c (output of chunk c) and MMA1(c+1)
-            // over keys 0-63 plus the lookahead term; warp 0 issues MMA1(c+1) over keys
-            // 64-127 and then the output tile's TMA store.  Each commits to BAR_D1 once per
-            // EMIT generation (phase c+1), with or without MMAs (see warp 11).
+            // ---- after EMIT(c): warp 12 issues MMA1(c+1) over keys 0-63 plus the lookahead
+            // term (the output term Mq_c delta_c goes with the state update); warp 0 issues
+            // MMA1(c+1) over keys 64-127 and then the output tile's TMA store.  Each commits
+            // to BAR_D1 once per EMIT generation (phase c+1), with or without MMAs (see
+            // warp 11).
             const int kh = warp == 12 ? 0 : 1;
             auto mma1 = [&](int c) {
                 const uint32_t d = tmem + kColD1 + kD1Buf * (c & 1) + 32u * kh;
@@ -720,9 +726,6 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (!live && lane == 0) *k2fail = 1;
                 tc_fence_after();
                 if (elect_one()) {
-                    if (live && kh == 0 && with_out)
-                        mma_ts(tmem + kColD1 + kD1Buf * (c & 1) + 16, tmem + kColDA + 8u * (c & 1),
-                               sdesc(stage(c) + kB3, kLbo, kSboB3), idesc16, 1);
                     if (live && has_next) mma1(c + 1);
                     tc_commit(bar(BAR_D1));
                 }
