@@ -38,11 +38,11 @@
 //     shared::cluster copy that completes the K2 CTA's barrier.
 //   CTA rank 1 ("K2 CTA"): warps 1-8 run the state chain (decay and bf16 copy of the
 //     state, delta, output rows) and only arrive on two named barriers; warp 11 issues
-//     the state update and the Mq term, warps 12 and 0 MMA1 of the next chunk (the
+//     the state update and the Mq term, warps 12 and 9 MMA1 of the next chunk (the
 //     tensor pipe runs one thread's MMAs in order but overlaps different threads'), warp
-//     0 also owns TMEM and issues the output tiles' TMA stores; warp 10 computes
-//     [P ; R] ahead of the chain; warp 9 relays copy landings back to the K1 groups and
-//     publishes how many chunks have landed.
+//     9 also issues the output tiles' TMA stores; warp 10 computes [P ; R] ahead of the
+//     chain; warp 0 owns TMEM, relays copy landings back to the K1 groups and publishes
+//     how many chunks have landed.
 // Splitting a chain over two SMs doubles the shared-memory bandwidth and issue slots
 // each chunk gets; one SM alone was bound by its shared-memory pipe.
 // Every wait is bounded: on exhaustion the kernel records KDA_ERR_DEVICE_TIMEOUT in the
@@ -145,6 +145,13 @@ static_assert(BAR_K2_END <= kNumBars, "too many barriers");
 constexpr uint32_t kNamedIssue = 1;  // delta_c and D_{c+1} written: state update, Mq
 constexpr uint32_t kNamedEmit = 2;   // output of chunk c-1 read, bf16 D_{c+1} written: MMA1(c+1)
 constexpr uint32_t kChainThreads = 256, kIssueCount = kChainThreads + 32, kEmitCount = kChainThreads + 64;
+// K2 CTA roles outside the chain (warps 1-8).  A warp runs on SM sub-partition
+// warp % 4: the two MMA1 issuers (12, 9) sit on different ones, so they issue in parallel.
+constexpr int kRelayWarp = 0;      // copy relay (and the TMEM allocation)
+constexpr int kPRWarp = 10;        // [P ; R] operands
+constexpr int kUpdateWarp = 11;    // state update and output term
+constexpr int kMma1WarpA = 12;     // MMA1 keys 0-63 and the lookahead term
+constexpr int kMma1WarpB = 9;      // MMA1 keys 64-127 and the output tiles' TMA stores
 
 __device__ __forceinline__ uint32_t b1_off(int n, int k) {
     return (n >> 3) * kSboB1 + (k >> 3) * kLbo + (n & 7) * 16 + (k & 7) * 2;
@@ -305,6 +312,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const uint32_t nbar = 1 + gi;     // named barrier of the group
         const int kt = tid - 32 - 128 * gi;
         const int kw = kt >> 5;           // warp within the group
+        // Phase-2 role of this warp, rotated by group: a CTA's warp w runs on SM
+        // sub-partition w % 4, so rotating puts the three groups' solve warps (role 0) on
+        // three different sub-partitions instead of one.
+        const int kr = (kw + gi) & 3;
         const int pc = kt & 63;           // channel pair: channels 2pc, 2pc+1
         const int hr = kt >> 6;           // row half: rows 8hr .. 8hr+7
         unsigned char* grp = smem + kSmGrp + gi * kGrpBytes;
@@ -403,14 +414,14 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (hr == 0) reinterpret_cast<float2*>(ob + kGC)[pc] = gcl;
             }
 
-            // Phase 2: warp 0 Gram A and the WY solve; warp 1 Gram Mq; warps 2-3 write
+            // Phase 2 (by role kr): 0 Gram A and the WY solve; 1 Gram Mq; 2-3 write
             // Qtil = (Q o exp(gam - gam_ref)) exp(gam_ref) into rows 16..31 of B1.
-            if (kw == 0 || (kw == 1 && with_out)) {
+            if (kr == 0 || (kr == 1 && with_out)) {
                 float acc[2][4];
-                gram16(smem_u32(st + (kw == 0 ? ST_KQ : ST_QQ) * kStArr),
+                gram16(smem_u32(st + (kr == 0 ? ST_KQ : ST_QQ) * kStArr),
                        smem_u32(st + ST_KK * kStArr), lane, acc);
                 const int g = lane >> 2, t = lane & 3;
-                if (kw == 0) {
+                if (kr == 0) {
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -456,8 +467,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             *reinterpret_cast<uint32_t*>(b3 + b3_off(r, sc)) = pack_bf16(m0, m1);
                         }
                 }
-            } else if (kw >= 2 && with_out) {
-                const int ct = kt - 64;  // 0..63
+            } else if (kr >= 2 && with_out) {
+                const int ct = 32 * (kr - 2) + lane;  // 0..63
                 unsigned char* b1 = ob + kB1;
 #pragma unroll
                 for (int e = ct; e < 256; e += 64) {
@@ -517,9 +528,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             fence_proxy_async_smem();
             named_bar_sync(nbar, 128);
-            // A thread of the group's last warp ships the chunk while thread 0 already
-            // waits for the next chunk's input tiles.
-            if (kt == 96) {
+            // A thread of the role-3 warp ships the chunk while thread 0 already waits for
+            // the next chunk's input tiles (role 3 is never warp 0 of the group: gi < 3).
+            if (kr == 3 && lane == 0) {
                 // Ship the chunk's operands into the K2 CTA's receive stage.
                 const int os = c % kRecvStages;
                 bool free_ok = c < kRecvStages ||
@@ -547,11 +558,11 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         //   warps 1-8   state chain: D_{c+1} = decay of S_c (fp32, and its bf16 copy),
         //               delta_c, then the output of chunk c-1;
         //   warp 11     S += Kbar_c^T delta_c and the Mq delta_c output term (after delta_c);
-        //   warps 12, 0 MMA1(c+1) over the two K halves, plus the lookahead term
+        //   warps 12, 9 MMA1(c+1) over the two K halves, plus the lookahead term
         //               delta_c [P_c ; R_c]^T (after the output of chunk c-1 was read);
-        //               warp 12 also issues the output tiles' TMA stores;
+        //               warp 9 also issues the output tiles' TMA stores;
         //   warp 10     [P_c ; R_c] with mma.sync, ahead of the chain;
-        //   warp 9      tells each K1 group when its bulk copy has landed.
+        //   warp 0      tells each K1 group when its bulk copy has landed.
         volatile int32_t* k2fail = reinterpret_cast<volatile int32_t*>(smem + kSmK2Fail);
         const bool with_out = (p.flags & kFlagNoOutput) == 0;
         // Output heads and this cluster's output head, recomputed where used so that they
@@ -574,7 +585,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         auto landed_or_wait = [&](int c) { return ld_acquire_cta(landed) > c || k1_full(c); };
         if ((p.debug_flags & 1) && !mbar_wait(bar(BAR_NEVER), 0, lim)) *k2fail = 1;  // never signalled
 
-        if (warp == 9) {
+        if (warp == kRelayWarp) {
             // ---- copy relay
             if (lane == 0) {
                 for (int c = 0; c < nchunks; ++c) {
@@ -588,7 +599,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
             __syncwarp();
-        } else if (warp == 10) {
+        } else if (warp == kPRWarp) {
             // ---- [P_m ; R_m] = [W_{m+1} ; Qtil_{m+1}] Kbar_m^T (16x16 each, K = 128)
             for (int m = 0; m + 1 < nchunks; ++m) {
                 const int slot = m % kPRSlots;
@@ -654,7 +665,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     st_release_cta(pr_ready, m + 1);
                 }
             }
-        } else if (warp == 11) {
+        } else if (warp == kUpdateWarp) {
             // ---- state update S += Kbar_c^T delta_c
             // Every iteration commits, with or without MMAs: after a failure the commits
             // still pace the chain one generation at a time.
@@ -679,13 +690,13 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (live && c > 0 && lane == 0)
                     mbar_arrive_remote_relaxed(mapa(bar(BAR_OUT_FREE + (c - 1) % kRecvStages), 0));
             }
-        } else if (warp == 12 || warp == 0) {
+        } else if (warp == kMma1WarpA || warp == kMma1WarpB) {
             // ---- after EMIT(c): warp 12 issues MMA1(c+1) over keys 0-63 plus the lookahead
-            // term (the output term Mq_c delta_c goes with the state update); warp 0 issues
+            // term (the output term Mq_c delta_c goes with the state update); warp 9 issues
             // MMA1(c+1) over keys 64-127 and then the output tile's TMA store.  Each commits
             // to BAR_D1 once per EMIT generation (phase c+1), with or without MMAs (see
             // warp 11).
-            const int kh = warp == 12 ? 0 : 1;
+            const int kh = warp == kMma1WarpA ? 0 : 1;
             auto mma1 = [&](int c) {
                 const uint32_t d = tmem + kColD1 + kD1Buf * (c & 1) + 32u * kh;
                 const uint32_t b1 = stage(c) + kB1;
@@ -801,7 +812,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                 for (int r = 0; r < 8; ++r) v[r] = __uint_as_float(a[r]) + __uint_as_float(b[r]);
             };
-            // Output rows 8hf.. of chunk cp: through an output tile (stored by warp 12), or
+            // Output rows 8hf.. of chunk cp: through an output tile (stored by warp 9), or
             // with plain stores (the last chunk of the sequence, possibly ragged).
             auto emit_out = [&](int cp, bool tile_ok) {
                 const int64_t t0p = bos + (int64_t)cp * kChunk;
@@ -913,7 +924,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tmem_wait_ld();
         }
         // Every MMA the three issuers started completes before TMEM is released.
-        if (warp == 0 || warp == 11 || warp == 12) {
+        if (warp == kMma1WarpA || warp == kMma1WarpB || warp == kUpdateWarp) {
             if (elect_one()) tc_commit(bar(BAR_DRAIN));
             __syncwarp();
             if (!mbar_wait(bar(BAR_DRAIN), 0, kDrainLimit) && lane == 0) record(p.status, kStatusTimeout);
