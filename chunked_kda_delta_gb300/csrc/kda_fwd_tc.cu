@@ -38,9 +38,9 @@
 //     shared::cluster copy that completes the K2 CTA's barrier.
 //   CTA rank 1 ("K2 CTA"): warps 1-8 run the state chain (decay and bf16 copy of the
 //     state, delta, output rows) and only arrive on two named barriers; warp 11 issues
-//     the state update and the Mq term, warps 12 and 9 MMA1 of the next chunk (the
+//     the state update and the Mq term, warps 10 and 9 MMA1 of the next chunk (the
 //     tensor pipe runs one thread's MMAs in order but overlaps different threads'), warp
-//     9 also issues the output tiles' TMA stores; warp 10 computes [P ; R] ahead of the
+//     9 also issues the output tiles' TMA stores; warp 12 computes [P ; R] ahead of the
 //     chain; warp 0 owns TMEM, relays copy landings back to the K1 groups and publishes
 //     how many chunks have landed.
 // Splitting a chain over two SMs doubles the shared-memory bandwidth and issue slots
@@ -146,11 +146,12 @@ constexpr uint32_t kNamedIssue = 1;  // delta_c and D_{c+1} written: state updat
 constexpr uint32_t kNamedEmit = 2;   // output of chunk c-1 read, bf16 D_{c+1} written: MMA1(c+1)
 constexpr uint32_t kChainThreads = 256, kIssueCount = kChainThreads + 32, kEmitCount = kChainThreads + 64;
 // K2 CTA roles outside the chain (warps 1-8).  A warp runs on SM sub-partition
-// warp % 4: the two MMA1 issuers (12, 9) sit on different ones, so they issue in parallel.
+// warp % 4: the two MMA1 issuers (10, 9) sit on different ones, so they issue in parallel,
+// and the busy [P ; R] warp shares sub-partition 0 with the nearly idle relay.
 constexpr int kRelayWarp = 0;      // copy relay (and the TMEM allocation)
-constexpr int kPRWarp = 10;        // [P ; R] operands
+constexpr int kPRWarp = 12;        // [P ; R] operands
 constexpr int kUpdateWarp = 11;    // state update and output term
-constexpr int kMma1WarpA = 12;     // MMA1 keys 0-63 and the lookahead term
+constexpr int kMma1WarpA = 10;     // MMA1 keys 0-63 and the lookahead term
 constexpr int kMma1WarpB = 9;      // MMA1 keys 64-127 and the output tiles' TMA stores
 
 __device__ __forceinline__ uint32_t b1_off(int n, int k) {
@@ -314,8 +315,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int kw = kt >> 5;           // warp within the group
         // Phase-2 role of this warp, rotated by group: a CTA's warp w runs on SM
         // sub-partition w % 4, so rotating puts the three groups' solve warps (role 0) on
-        // three different sub-partitions instead of one.
-        const int kr = (kw + gi) & 3;
+        // sub-partitions 1, 2 and 3 (the producer has 0) and their Mq warps next to them.
+        const int kr = (kw - gi) & 3;
         const int pc = kt & 63;           // channel pair: channels 2pc, 2pc+1
         const int hr = kt >> 6;           // row half: rows 8hr .. 8hr+7
         unsigned char* grp = smem + kSmGrp + gi * kGrpBytes;
@@ -528,9 +529,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             fence_proxy_async_smem();
             named_bar_sync(nbar, 128);
-            // A thread of the role-3 warp ships the chunk while thread 0 already waits for
-            // the next chunk's input tiles (role 3 is never warp 0 of the group: gi < 3).
-            if (kr == 3 && lane == 0) {
+            // A thread of the group's last warp (never its solve warp: that is warp gi < 3)
+            // ships the chunk while thread 0 already waits for the next chunk's input tiles.
+            if (kt == 96) {
                 // Ship the chunk's operands into the K2 CTA's receive stage.
                 const int os = c % kRecvStages;
                 bool free_ok = c < kRecvStages ||
@@ -558,10 +559,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         //   warps 1-8   state chain: D_{c+1} = decay of S_c (fp32, and its bf16 copy),
         //               delta_c, then the output of chunk c-1;
         //   warp 11     S += Kbar_c^T delta_c and the Mq delta_c output term (after delta_c);
-        //   warps 12, 9 MMA1(c+1) over the two K halves, plus the lookahead term
+        //   warps 10, 9 MMA1(c+1) over the two K halves, plus the lookahead term
         //               delta_c [P_c ; R_c]^T (after the output of chunk c-1 was read);
         //               warp 9 also issues the output tiles' TMA stores;
-        //   warp 10     [P_c ; R_c] with mma.sync, ahead of the chain;
+        //   warp 12     [P_c ; R_c] with mma.sync, ahead of the chain;
         //   warp 0      tells each K1 group when its bulk copy has landed.
         volatile int32_t* k2fail = reinterpret_cast<volatile int32_t*>(smem + kSmK2Fail);
         const bool with_out = (p.flags & kFlagNoOutput) == 0;
@@ -691,7 +692,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     mbar_arrive_remote_relaxed(mapa(bar(BAR_OUT_FREE + (c - 1) % kRecvStages), 0));
             }
         } else if (warp == kMma1WarpA || warp == kMma1WarpB) {
-            // ---- after EMIT(c): warp 12 issues MMA1(c+1) over keys 0-63 plus the lookahead
+            // ---- after EMIT(c): warp 10 issues MMA1(c+1) over keys 0-63 plus the lookahead
             // term (the output term Mq_c delta_c goes with the state update); warp 9 issues
             // MMA1(c+1) over keys 64-127 and then the output tile's TMA store.  Each commits
             // to BAR_D1 once per EMIT generation (phase c+1), with or without MMAs (see
