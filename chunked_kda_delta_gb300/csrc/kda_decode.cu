@@ -31,16 +31,20 @@ __device__ __forceinline__ void state_load(const float* p, float (&x)[4]) {
 __device__ __forceinline__ void state_store(float* p, const float (&x)[4]) {
     __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
 }
+// kGrouped: unequal head counts (HeadMap); the equal-count instance keeps plain head
+// indexing (the map's arithmetic costs the bf16 kernel spills at its register cap).
+template <bool kGrouped>
 __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_kernel(const DecodeParams p) {
     __shared__ float s_k[kD], s_q[kD], s_e[kD], s_v[kD], s_d[kD];
     __shared__ __align__(16) float s_red[2][kDecThreads / 32][kD];
     __shared__ float s_qk[kDecThreads / 32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int Ho = p.Hq > p.H ? p.Hq : p.H, Hk = p.Hq > p.H ? p.H : p.Hq;
+    const int Hq = kGrouped ? p.Hq : p.H;
+    const int Ho = Hq > p.H ? Hq : p.H, Hk = Hq > p.H ? p.H : Hq;
     const int64_t n = (int64_t)blockIdx.x / Ho;
     const int ho = (int)(blockIdx.x % Ho);
-    const HeadMap hm = head_map(ho, p.H, p.Hq);
+    const HeadMap hm = kGrouped ? head_map(ho, p.H, Hq) : HeadMap{ho, ho, ho, true};
     const int r0 = warp * kDecRows, c0 = lane * 4;
     const size_t soff = ((size_t)n * p.H + hm.hs) * kD * kD + (size_t)r0 * kD + c0;
 
@@ -62,7 +66,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) kda_decode_kernel(const Decode
         float beta_t = 0.f;
         if (tid < kD) {
             s_k[tid] = __bfloat162float(p.k[(tok * Hk + hm.hk) * kD + tid]);
-            s_q[tid] = __bfloat162float(p.q[(tok * p.Hq + hm.hq) * kD + tid]);
+            s_q[tid] = __bfloat162float(p.q[(tok * Hq + hm.hq) * kD + tid]);
             s_v[tid] = __bfloat162float(p.v[row * kD + tid]);
             s_e[tid] = expf(p.g[row * kD + tid]);
             beta_t = __bfloat162float(p.beta[row]);
@@ -150,6 +154,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+template <bool kGrouped>
 __global__ void __launch_bounds__(kDecB16Threads, 3) kda_decode_bf16_kernel(const DecodeParams p) {
     __shared__ float s_k[kD], s_q[kD], s_e[kD], s_v[kD];
     __shared__ __align__(16) float s_d[kD];
@@ -158,10 +163,11 @@ __global__ void __launch_bounds__(kDecB16Threads, 3) kda_decode_bf16_kernel(cons
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hw = lane >> 4, c0 = (lane & 15) * 8;
-    const int Ho = p.Hq > p.H ? p.Hq : p.H, Hk = p.Hq > p.H ? p.H : p.Hq;
+    const int Hq = kGrouped ? p.Hq : p.H;
+    const int Ho = Hq > p.H ? Hq : p.H, Hk = Hq > p.H ? p.H : Hq;
     const int64_t n = (int64_t)blockIdx.x / Ho;
     const int ho = (int)(blockIdx.x % Ho);
-    const HeadMap hm = head_map(ho, p.H, p.Hq);
+    const HeadMap hm = kGrouped ? head_map(ho, p.H, Hq) : HeadMap{ho, ho, ho, true};
     const int rbase = warp * 32 + hw;  // this thread's rows: rbase + 2 i
     const size_t soff = ((size_t)n * p.H + hm.hs) * kD * kD + (size_t)rbase * kD + c0;
 
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(kDecB16Threads, 3) kda_decode_bf16_kernel(cons
         const size_t tok = (size_t)n * p.T + t;
         const size_t row = tok * p.H + hm.hs;
         s_k[tid] = __bfloat162float(p.k[(tok * Hk + hm.hk) * kD + tid]);
-        s_q[tid] = __bfloat162float(p.q[(tok * p.Hq + hm.hq) * kD + tid]);
+        s_q[tid] = __bfloat162float(p.q[(tok * Hq + hm.hq) * kD + tid]);
         s_v[tid] = __bfloat162float(p.v[row * kD + tid]);
         s_e[tid] = expf(p.g[row * kD + tid]);
         const float beta_t = __bfloat162float(p.beta[row]);
@@ -274,10 +280,18 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
     const int64_t rows = (int64_t)p.N * (p.Hq > p.H ? p.Hq : p.H);
     if (rows == 0) return cudaSuccess;
     const dim3 grid((unsigned)rows);
-    if (p.state_bf16)
-        kda_decode_bf16_kernel<<<grid, dim3(kDecB16Threads), 0, stream>>>(p);
-    else
-        kda_decode_kernel<<<grid, dim3(kDecThreads), 0, stream>>>(p);
+    const bool grouped = p.Hq != p.H;
+    if (p.state_bf16) {
+        if (grouped)
+            kda_decode_bf16_kernel<true><<<grid, dim3(kDecB16Threads), 0, stream>>>(p);
+        else
+            kda_decode_bf16_kernel<false><<<grid, dim3(kDecB16Threads), 0, stream>>>(p);
+    } else {
+        if (grouped)
+            kda_decode_kernel<true><<<grid, dim3(kDecThreads), 0, stream>>>(p);
+        else
+            kda_decode_kernel<false><<<grid, dim3(kDecThreads), 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 
