@@ -271,6 +271,12 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             return t < eos ? __bfloat162float(p.beta[t * H + h]) : 0.f;
         };
         float b_cur = load_beta(0), b_next = load_beta(1);
+        int hq = h, hk = h;  // q and k heads of this cluster, once
+        if (kGrouped) {
+            const HeadMap hm = head_map((int)((blockIdx.x >> 1) % (p.Hq > p.H ? p.Hq : p.H)), p.H, p.Hq);
+            hq = hm.hq;
+            hk = hm.hk;
+        }
         int issued = 0;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % kInStages;
@@ -289,12 +295,6 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (lane == 0) {
                 const int32_t t0 = (int32_t)(bos + (int64_t)c * kChunk);
                 mbar_arrive_expect_tx(bar(BAR_IN_FULL + s), kTxBytes);
-                int hq = h, hk = h;
-                if (kGrouped) {
-                    const HeadMap hm = head_map((int)((blockIdx.x >> 1) % (p.Hq > p.H ? p.Hq : p.H)), p.H, p.Hq);
-                    hq = hm.hq;
-                    hk = hm.hk;
-                }
                 tma_load_3d(dst + kInQ, &tm_q, bar(BAR_IN_FULL + s), 0, hq, t0);
                 tma_load_3d(dst + kInK, &tm_k, bar(BAR_IN_FULL + s), 0, hk, t0);
                 tma_load_3d(dst + kInV, &tm_v, bar(BAR_IN_FULL + s), 0, h, t0);
@@ -698,6 +698,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // to BAR_D1 once per EMIT generation (phase c+1), with or without MMAs (see
             // warp 11).
             const int kh = warp == kMma1WarpA ? 0 : 1;
+            const int tile_head = out_head();  // once: the tile stores below run every chunk
             auto mma1 = [&](int c) {
                 const uint32_t d = tmem + kColD1 + kD1Buf * (c & 1) + 32u * kh;
                 const uint32_t b1 = stage(c) + kB1;
@@ -748,7 +749,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     // commits later, so the drain below (all but the two newest stores)
                     // covers the store of the chunk four back, whose tile comes next.
                     const int32_t t0p = (int32_t)(bos + (int64_t)(c - 1) * kChunk);
-                    tma_store_3d(&tm_out, sbase + kSmOTile + ((c - 1) % kOTiles) * kOTileBytes, 0, out_head(), t0p);
+                    tma_store_3d(&tm_out, sbase + kSmOTile + ((c - 1) % kOTiles) * kOTileBytes, 0, tile_head, t0p);
                     bulk_commit();
                     bulk_wait_read<2>();
                 }
