@@ -317,6 +317,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // sub-partition w % 4, so rotating puts the three groups' solve warps (role 0) on
         // sub-partitions 1, 2 and 3 (the producer has 0) and their Mq warps next to them.
         const int kr = (kw - gi) & 3;
+        // The thread that waits on the group's barriers (input tiles, previous copy) is
+        // lane 0 of the group's warp (gi + 1) % 3: sub-partitions 2, 3 and 1 for groups 0,
+        // 1 and 2, and never the solve warp (gi) nor the shipping warp (3).
+        const int kt_wait = 32 * ((gi + 1) % 3);
         const int pc = kt & 63;           // channel pair: channels 2pc, 2pc+1
         const int hr = kt >> 6;           // row half: rows 8hr .. 8hr+7
         unsigned char* grp = smem + kSmGrp + gi * kGrpBytes;
@@ -333,9 +337,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int s = c % kInStages;
             // One thread waits for the input tiles; the group barrier publishes them.
             bool ok = !fail_flag[gi];
-            if (kt == 0) ok = ok && mbar_wait(bar(BAR_IN_FULL + s), (c / kInStages) & 1, lim);
+            if (kt == kt_wait) ok = ok && mbar_wait(bar(BAR_IN_FULL + s), (c / kInStages) & 1, lim);
             if (named_bar_or(nbar, 128, !ok)) {
-                if (kt == 0) record(p.status, kStatusTimeout);
+                if (kt == kt_wait) record(p.status, kStatusTimeout);
                 break;
             }
             const int64_t t0 = bos + (int64_t)c * kChunk;
@@ -398,13 +402,13 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // through the peer's barrier, which the K2 CTA relays back).  Waiting this late
             // gives that copy the whole of phase 1 to land.
             bool copied = true;
-            if (kt == 0 && c >= kK1Groups)
+            if (kt == kt_wait && c >= kK1Groups)
                 copied = mbar_wait(bar(BAR_COPIED + gi), ((c / kK1Groups) - 1) & 1, lim);
             if (named_bar_or(nbar, 128, !copied)) {
-                if (kt == 0) record(p.status, kStatusTimeout);
+                if (kt == kt_wait) record(p.status, kStatusTimeout);
                 break;
             }
-            if (kt == 0) mbar_arrive(bar(BAR_IN_EMPTY + s));  // input tiles consumed
+            if (kt == kt_wait) mbar_arrive(bar(BAR_IN_EMPTY + s));  // input tiles consumed
             {   // Kbar rows 2pc, 2pc+1 of B2 (N = key channel, K = chunk row), exp(gam_C)
                 unsigned char* b2 = ob + kB2;
                 const int c0 = 2 * pc, c1 = 2 * pc + 1;
@@ -530,7 +534,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             fence_proxy_async_smem();
             named_bar_sync(nbar, 128);
             // A thread of the group's last warp (never its solve warp: that is warp gi < 3)
-            // ships the chunk while thread 0 already waits for the next chunk's input tiles.
+            // ships the chunk while the waiting thread already waits for the next chunk's
+            // input tiles.
             if (kt == 96) {
                 // Ship the chunk's operands into the K2 CTA's receive stage.
                 const int os = c % kRecvStages;
