@@ -76,10 +76,7 @@ kda_status device_info(int dev, DeviceInfo** out) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kda::serial_smem_bytes())))
             return cuda_fail(e, "cudaFuncSetAttribute(grouped kernel)");
-        if ((e = cudaFuncSetAttribute(kda::merge_kernel_symbol(),
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kda::merge_smem_bytes())))
-            return cuda_fail(e, "cudaFuncSetAttribute(merge kernel)");
+        if ((e = kda::merge_init())) return cuda_fail(e, "cudaFuncSetAttribute(merge kernels)");
         {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2, 1, 1);
@@ -364,13 +361,14 @@ struct SegPlan {
 // Serial or segment mode, and the segment length, for a problem with `resident`
 // co-resident clusters.  Cost unit: one chunk period of one state chain.  Every pass of
 // the fused kernel (serial; segment summary, transition and output passes) costs about
-// the same per chunk on GB300 (T = 131072, H = 64: serial 0.925 us per chunk, the segment
-// passes 0.908 us per chunk of the busiest cluster slot), clusters beyond `resident` run
-// in further waves, and each segment adds a fixed cost (the merge walks a chain's
-// segments one after another; each short cluster fills its pipeline).  Fitted on GB300
-// from T = 131072, H = 4 with segments of 512 .. 8192 tokens (1.55 .. 4.99 ms against
-// 7.53 ms serial): about 15 chunk periods per segment, within 5% at every point.
-constexpr double kMergePerSegment = 15.0;
+// the same per chunk on GB300 (T = 131072: serial 0.82 us per chunk with 4 heads and
+// 0.88 us with 64, the segment passes 0.82 and 0.85 us per chunk of the busiest cluster
+// slot), clusters beyond `resident` run in further waves, and each segment adds a fixed
+// cost (the merge walks a chain's segments one after another; each short cluster fills
+// its pipeline).  Fitted on GB300 from T = 131072, H = 4 with segments of 512 .. 16384
+// tokens (1.32 .. 2.54 ms against 6.70 ms serial): about 5 chunk periods per segment,
+// within 3% at every point.
+constexpr double kMergePerSegment = 5.0;
 constexpr double kSegmentMargin = 0.8;      // segment mode must win by 20%
 constexpr size_t kPlanWorkspaceCap = (size_t)4 << 30;
 
@@ -519,7 +517,8 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
             ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0 | kda::kFlagSkipLastSeg;
             if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
                 return cuda_fail(e, "pre_scan (transition) launch");
-            if ((e = kda::launch_merge(m_seg, b_seg, s0, carries, pr.N, 0, pr.H, stream, table)) !=
+            if ((e = kda::launch_merge(m_seg, b_seg, s0, carries, pr.N, 0, pr.H, di->sm_count, stream,
+                                      table)) !=
                 cudaSuccess)
                 return cuda_fail(e, "merge launch");
             kda::FwdParams pk = p;
@@ -560,7 +559,7 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
     ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0;
     if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
         return cuda_fail(e, "pre_scan (transition) launch");
-    if ((e = kda::launch_merge(m_seg, b_seg, s0, carries, pr.N, sp.nseg, pr.H, stream)) !=
+    if ((e = kda::launch_merge(m_seg, b_seg, s0, carries, pr.N, sp.nseg, pr.H, di->sm_count, stream)) !=
         cudaSuccess)
         return cuda_fail(e, "merge launch");
     kda::FwdParams pk = p;
@@ -942,7 +941,7 @@ extern "C" kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const 
     if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
         return cuda_fail(e, "pre_scan (transition) launch");
     if ((e = kda::launch_merge(m_seg, b_seg, initial_state, carries, pr.N, sp.nseg, pr.H,
-                               stream)) != cudaSuccess)
+                               di->sm_count, stream)) != cudaSuccess)
         return cuda_fail(e, "merge launch");
     kda::FwdParams pk = p;
     pk.seg_len = segment_len;

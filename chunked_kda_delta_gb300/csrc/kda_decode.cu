@@ -1,9 +1,9 @@
 // kda_decode.cu -- the recurrent decode step: a few tokens (typically one) per
 // (sequence, head), applied to a resident state with fp32 or bf16 storage.
 //
-// Per token (the gated delta rule with per-channel decay, cuLA PR #103 "feat(kda/sm90):
-// FlashKDA prefill port + intracard-CP prefill", problem statement; the same
-// recurrence the prefill computes chunkwise):
+// Per token (Kimi Delta Attention: the gated delta rule with a per-channel decay, the
+// method cuLA PR #103 "feat(kda/sm90): FlashKDA prefill port + intracard-CP prefill"
+// computes chunkwise; the same recurrence the prefill computes):
 //     S' = Diag(exp g) S,   u = S'^T k,   delta = beta (v - u),
 //     S  = S' + k delta^T,  o = scale S^T q = scale (S'^T q + (q . k) delta).
 // The last form needs one pass over the state for both reductions (u and S'^T q);

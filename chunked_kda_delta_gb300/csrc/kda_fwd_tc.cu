@@ -3,8 +3,9 @@
 // in tensor memory (TMEM) across all chunks.
 //
 // The method (cuLA PR #103 "feat(kda/sm90): FlashKDA prefill port + intracard-CP
-// prefill", commit notes: "K1 prepares decayed q/k, beta and the WY inverse; K2 runs
-// the inter-chunk recurrence. CHUNK=16, D=128, forward only").  For a chunk of C <= 16
+// prefill", commit notes): two stages, forward only, chunks of 16 tokens and head size
+// 128; K1 builds the decayed q/k, applies beta and forms the WY inverse of each chunk,
+// and K2 carries the state from chunk to chunk.  For a chunk of C <= 16
 // rows with chunk-start state S (Dk x Dv = 128 x 128) and in-chunk cumulative
 // log-decay gam_r = sum_{m<=r} g_m (per channel):
 //   A      = strict_lower(beta_r (k_r . k_s exp(gam_r - gam_s)))      16x16

@@ -169,16 +169,17 @@ cudaError_t launch_segment_table(const int32_t* cu, int32_t N, int64_t T_total, 
                                  int32_t* seg_start, int32_t* status, cudaStream_t stream);
 // Dense: B sequences of nseg segments.  Varlen (seg_start != nullptr): B = N sequences,
 // each with its own count from the table; summaries and carries indexed by segment row.
+// The carry's columns are split over merge_block_cols(B, H, sm_count)-wide blocks.
 cudaError_t launch_merge(const float* m_seg, const float* b_seg, const float* s0, float* carries,
-                         int32_t B, int32_t nseg, int32_t H, cudaStream_t stream,
+                         int32_t B, int32_t nseg, int32_t H, int sm_count, cudaStream_t stream,
                          const int32_t* seg_start = nullptr);
+int merge_block_cols(int32_t B, int32_t H, int sm_count);
+cudaError_t merge_init();  // shared-memory limits of the merge kernels, once per device
 // Decode: one CTA per (sequence, head).
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 size_t serial_smem_bytes();
 int serial_block_threads();
 const void* serial_kernel_symbol();   // equal head counts
 const void* grouped_kernel_symbol();  // grouped heads (same shared memory and block size)
-size_t merge_smem_bytes();
-const void* merge_kernel_symbol();
 
 }  // namespace kda

@@ -1,37 +1,69 @@
 // kda_merge.cu -- the "merge" step of segment-parallel prefill: the serial combine of
 // per-segment summaries into the carry (state at each segment start).
 //
-// Segment pipeline (cuLA PR #103 "feat(kda/sm90): FlashKDA prefill port + intracard-CP
-// prefill", commit notes: "Split long sequences into segments and run the recurrence per
-// segment: K1 once -> pre_scan -> merge -> segment-K2").  Over one segment the state map
-// is affine, S_end = m_seg S_start + b_seg, so
+// Segment pipeline (cuLA PR #103, FlashKDA prefill port with intra-card context
+// parallelism, commit notes): a long sequence is cut into segments; K1 runs once, a
+// pre_scan summarises every segment, the merge below chains the summaries, and a second
+// K2 pass runs each segment from its carry.  Over one segment the state map is affine,
+// S_end = m_seg S_start + b_seg, so
 //     carry_0 = S_0 (or 0),   carry_{s+1} = m_seg[s] carry_s + b_seg[s].
-// One CTA per (sequence, head, 32-column block of the carry): the carry's columns are
-// independent, so each CTA runs the whole serial chain over segments for its block.
+// One CTA per (sequence, head, column block of the carry): the carry's columns are
+// independent, so each CTA runs the whole serial chain over segments for its block.  The
+// next segment's transition and summary block stream into a second shared-memory buffer
+// (16-byte cp.async) while the current product runs, so a step of the chain waits on no
+// global load.  The block width is the widest of 32 / 16 / 8 columns that still gives
+// every SM a CTA, so that few heads spread over the GPU.
 // fp32 throughout (the carries feed every later output of their segment).
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kCols = 32;             // carry columns per CTA
-constexpr int kMRow = kD + 4;         // padded row of the transposed transition in smem
-constexpr int kCRow = kCols + 4;      // padded row of the carry block
-constexpr int kMergeSmem = (kD * kMRow + kD * kCRow) * 4;
+constexpr int kMergeThreads = 256;
+constexpr int kMRow = kD + 4;  // padded row of a transition in shared memory
 
-__global__ void __launch_bounds__(256)
+template <int kCols>
+struct MergeShape {
+    static constexpr int kColGroups = kCols / 4;                   // float4 columns
+    static constexpr int kRowGroups = kMergeThreads / kColGroups;  // threads along rows
+    static constexpr int kRowsPer = kD / kRowGroups;               // rows per thread
+    static constexpr int kBRow = kCols + 4;                        // padded row of a block
+    static constexpr int kMFloats = kD * kMRow;
+    static constexpr int kBFloats = kD * kBRow;
+    // two transitions, two summary blocks, the carry block
+    static constexpr int kSmem = (2 * kMFloats + 3 * kBFloats) * 4;
+};
+
+__device__ __forceinline__ void cp_async16(float* sdst, const float* gsrc) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(sdst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+template <int kCols>
+__global__ void __launch_bounds__(kMergeThreads)
 kda_merge_kernel(const float* __restrict__ m_seg, const float* __restrict__ b_seg,
                  const float* __restrict__ s0, float* __restrict__ carries, int B, int nseg,
                  int H, const int32_t* __restrict__ seg_start) {
+    using S = MergeShape<kCols>;
     extern __shared__ __align__(16) float sm[];
-    float* Mt = sm;                  // Mt[k][i] = m[i][k]
-    float* Cb = sm + kD * kMRow;     // carry block [k][c]
+    float* Ms = sm;                        // two transitions m[i][k], rows padded
+    float* Bsm = sm + 2 * S::kMFloats;     // two summary blocks b[i][c]
+    float* Cb = Bsm + 2 * S::kBFloats;     // carry block [k][c]
     const int tid = threadIdx.x;
-    const int cb = blockIdx.x % (kD / kCols);
-    const int h = (blockIdx.x / (kD / kCols)) % H;
-    const int b = blockIdx.x / ((kD / kCols) * H);
-    const int i0 = (tid >> 3) * 4;   // 4 rows
-    const int c0 = (tid & 7) * 4;    // 4 columns of the block
+    constexpr int kBlocks = kD / kCols;
+    const int cb = blockIdx.x % kBlocks;
+    const int h = (blockIdx.x / kBlocks) % H;
+    const int b = blockIdx.x / (kBlocks * H);
+    // Thread tile: rows rg + kRowGroups*a (a < kRowsPer), columns c0..c0+3 of the block.
+    // A warp's rows are consecutive, so its float4 reads of a padded transition row fall
+    // on distinct banks; its columns are consecutive float4s of one carry row.
+    const int rg = tid / S::kColGroups;
+    const int c0 = (tid % S::kColGroups) * 4;
     const size_t st = (size_t)kD * kD;
     // Dense: summaries [B][nseg-1][H], carries [B][nseg][H].  Varlen: every table indexed
     // by the global segment row g = seg_start[b] + s, sequence b owning its own count.
@@ -41,71 +73,132 @@ kda_merge_kernel(const float* __restrict__ m_seg, const float* __restrict__ b_se
         g0 = (size_t)seg_start[b];
         ns = seg_start[b + 1] - seg_start[b];
     }
+    if (ns <= 0) return;  // malformed cu_seqlens: the table is all zeros and nothing runs
     auto carry_at = [&](int s) {
         return carries + ((seg_start ? g0 + s : (size_t)b * nseg + s) * H + h) * st;
     };
     auto summary_at = [&](const float* base, int s) {
         return base + ((seg_start ? g0 + s : (size_t)b * (nseg - 1) + s) * H + h) * st;
     };
+    auto prefetch = [&](int s, int buf) {
+        const float* M = summary_at(m_seg, s);
+        const float* Bs = summary_at(b_seg, s) + cb * kCols;
+        float* Md = Ms + buf * S::kMFloats;
+        float* Bd = Bsm + buf * S::kBFloats;
+        for (int e = tid; e < kD * (kD / 4); e += kMergeThreads) {
+            const int i = e / (kD / 4), j = e % (kD / 4);
+            cp_async16(Md + i * kMRow + 4 * j, M + (size_t)i * kD + 4 * j);
+        }
+        for (int e = tid; e < kD * S::kColGroups; e += kMergeThreads) {
+            const int i = e / S::kColGroups, j = e % S::kColGroups;
+            cp_async16(Bd + i * S::kBRow + 4 * j, Bs + (size_t)i * kD + 4 * j);
+        }
+        cp_async_commit();
+    };
 
+    if (ns > 1) prefetch(0, 0);
     // carry_0
-    for (int e = tid; e < kD * kCols; e += 256) {
+    for (int e = tid; e < kD * kCols; e += kMergeThreads) {
         const int k = e / kCols, c = e % kCols;
         const float v = s0 ? s0[((size_t)b * H + h) * st + (size_t)k * kD + cb * kCols + c] : 0.f;
-        Cb[k * kCRow + c] = v;
+        Cb[k * S::kBRow + c] = v;
         carry_at(0)[(size_t)k * kD + cb * kCols + c] = v;
     }
     for (int s = 0; s + 1 < ns; ++s) {
-        const float* M = summary_at(m_seg, s);
-        const float* Bs = summary_at(b_seg, s);
-        for (int e = tid; e < kD * kD; e += 256) {
-            const int i = e / kD, k = e % kD;
-            Mt[k * kMRow + i] = M[e];
+        // Buffer (s+1)&1 was last read in step s-1, which ended on a barrier.
+        if (s + 2 < ns) {
+            prefetch(s + 1, (s + 1) & 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
-        __syncthreads();
-        float acc[4][4];
+        __syncthreads();  // step s's buffers and the carry block written in step s-1
+        const float* Mb = Ms + (s & 1) * S::kMFloats;
+        const float* Bb = Bsm + (s & 1) * S::kBFloats;
+        float acc[S::kRowsPer][4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                acc[a][c] = Bs[(size_t)(i0 + a) * kD + cb * kCols + c0 + c];
-#pragma unroll 4
-        for (int k = 0; k < kD; ++k) {
-            const float4 mv = *reinterpret_cast<const float4*>(Mt + k * kMRow + i0);
-            const float4 cv = *reinterpret_cast<const float4*>(Cb + k * kCRow + c0);
-            const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-            const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(mm[a], cc[c], acc[a][c]);
+        for (int a = 0; a < S::kRowsPer; ++a) {
+            const float4 bv = *reinterpret_cast<const float4*>(Bb + (rg + S::kRowGroups * a) * S::kBRow + c0);
+            acc[a][0] = bv.x;
+            acc[a][1] = bv.y;
+            acc[a][2] = bv.z;
+            acc[a][3] = bv.w;
         }
-        __syncthreads();
+#pragma unroll 2
+        for (int k = 0; k < kD; k += 4) {
+            float mm[S::kRowsPer][4];
+#pragma unroll
+            for (int a = 0; a < S::kRowsPer; ++a) {
+                const float4 mv = *reinterpret_cast<const float4*>(Mb + (rg + S::kRowGroups * a) * kMRow + k);
+                mm[a][0] = mv.x;
+                mm[a][1] = mv.y;
+                mm[a][2] = mv.z;
+                mm[a][3] = mv.w;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 cv = *reinterpret_cast<const float4*>(Cb + (k + kk) * S::kBRow + c0);
+#pragma unroll
+                for (int a = 0; a < S::kRowsPer; ++a) {
+                    acc[a][0] = fmaf(mm[a][kk], cv.x, acc[a][0]);
+                    acc[a][1] = fmaf(mm[a][kk], cv.y, acc[a][1]);
+                    acc[a][2] = fmaf(mm[a][kk], cv.z, acc[a][2]);
+                    acc[a][3] = fmaf(mm[a][kk], cv.w, acc[a][3]);
+                }
+            }
+        }
+        __syncthreads();  // every read of the carry block and of buffer s&1 is done
         float* out = carry_at(s + 1);
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            *reinterpret_cast<float4*>(Cb + (i0 + a) * kCRow + c0) =
-                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-            *reinterpret_cast<float4*>(out + (size_t)(i0 + a) * kD + cb * kCols + c0) =
-                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        for (int a = 0; a < S::kRowsPer; ++a) {
+            const int i = rg + S::kRowGroups * a;
+            const float4 o = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+            *reinterpret_cast<float4*>(Cb + i * S::kBRow + c0) = o;
+            *reinterpret_cast<float4*>(out + (size_t)i * kD + cb * kCols + c0) = o;
         }
-        __syncthreads();
     }
+}
+
+template <int kCols>
+cudaError_t merge_set_smem() {
+    return cudaFuncSetAttribute(kda_merge_kernel<kCols>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                MergeShape<kCols>::kSmem);
+}
+
+template <int kCols>
+cudaError_t merge_launch(const float* m_seg, const float* b_seg, const float* s0, float* carries,
+                         int32_t B, int32_t nseg, int32_t H, cudaStream_t stream,
+                         const int32_t* seg_start) {
+    const long long blocks = (long long)B * H * (kD / kCols);
+    kda_merge_kernel<kCols><<<(unsigned)blocks, kMergeThreads, MergeShape<kCols>::kSmem, stream>>>(
+        m_seg, b_seg, s0, carries, B, nseg, H, seg_start);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t merge_smem_bytes() { return kMergeSmem; }
-const void* merge_kernel_symbol() { return reinterpret_cast<const void*>(&kda_merge_kernel); }
+cudaError_t merge_init() {
+    cudaError_t e;
+    if ((e = merge_set_smem<32>()) || (e = merge_set_smem<16>()) || (e = merge_set_smem<8>())) return e;
+    return cudaSuccess;
+}
+
+int merge_block_cols(int32_t B, int32_t H, int sm_count) {
+    const long long heads = (long long)B * H;
+    if (heads * (kD / 32) >= sm_count) return 32;
+    if (heads * (kD / 16) >= sm_count) return 16;
+    return 8;
+}
 
 cudaError_t launch_merge(const float* m_seg, const float* b_seg, const float* s0, float* carries,
-                         int32_t B, int32_t nseg, int32_t H, cudaStream_t stream,
+                         int32_t B, int32_t nseg, int32_t H, int sm_count, cudaStream_t stream,
                          const int32_t* seg_start) {
-    const long long blocks = (long long)B * H * (kD / kCols);
-    if (blocks == 0) return cudaSuccess;
-    kda_merge_kernel<<<(unsigned)blocks, 256, kMergeSmem, stream>>>(m_seg, b_seg, s0, carries, B,
-                                                                   nseg, H, seg_start);
-    return cudaGetLastError();
+    if ((long long)B * H == 0) return cudaSuccess;
+    switch (merge_block_cols(B, H, sm_count)) {
+        case 32: return merge_launch<32>(m_seg, b_seg, s0, carries, B, nseg, H, stream, seg_start);
+        case 16: return merge_launch<16>(m_seg, b_seg, s0, carries, B, nseg, H, stream, seg_start);
+        default: return merge_launch<8>(m_seg, b_seg, s0, carries, B, nseg, H, stream, seg_start);
+    }
 }
 
 // One CTA: validate cu_seqlens (cu[0] = 0, non-decreasing, cu[N] <= T_total), then an

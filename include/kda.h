@@ -182,8 +182,9 @@ kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q
 
 /* kda_decode -- the recurrent step for a few tokens (typically one) of each sequence,
  * the inner step of autoregressive decoding: per (sequence, head) and token, the
- * recurrence at the top of this header (cuLA PR #103 "feat(kda/sm90): FlashKDA
- * prefill port + intracard-CP prefill", problem statement), applied token by token to
+ * recurrence at the top of this header (Kimi Delta Attention: the gated delta rule
+ * with a per-channel decay, the method cuLA PR #103 "feat(kda/sm90): FlashKDA prefill
+ * port + intracard-CP prefill" computes chunkwise), applied token by token to
  * a state that stays resident on the device.  The pages mention a decode registration
  * beside the prefill (flashinfer PR #4313 "feat(cake_kda): share recurrent prefill
  * kernels across SM100 family", publication notes) and a bf16 final state in the

@@ -12,11 +12,12 @@ arrays.  Three forms of the same definition are exposed:
 * :func:`recurrent` -- the KDA recurrence token by token,
   ``S_t = (I - b_t k_t k_t^T) Diag(exp g_t) S_{t-1} + b_t k_t v_t^T``,
   ``o_t = scale S_t^T q_t``.
-* :func:`chunked` -- the chunkwise WY form (stage "K1 prepares decayed q/k,
-  beta and the WY inverse; K2 runs the inter-chunk recurrence", CHUNK=16).
-* :func:`segmented` -- the segment pipeline "K1 once -> pre_scan -> merge ->
-  segment-K2" (cuLA PR #103, "feat(kda/sm90): FlashKDA prefill port +
-  intracard-CP prefill", commit notes).
+* :func:`chunked` -- the chunkwise WY form, chunks of 16 tokens: decayed q/k,
+  beta and the WY inverse per chunk (K1), then the state carried from chunk to
+  chunk (K2).
+* :func:`segmented` -- the segment pipeline: K1 once, per-segment summaries
+  (pre_scan), a serial merge of the carries, then K2 per segment (cuLA PR #103,
+  "feat(kda/sm90): FlashKDA prefill port + intracard-CP prefill", commit notes).
 * :func:`grouped` -- any form over grouped (unequal) head counts, by running every
   output head as a plain head on the tensors it reads.
 

@@ -13,12 +13,13 @@
  *     o_t = scale * S_t^T q_t
  *
  * with S in R^{Dk x Dv}, S_0 = initial state (or zero) and final = S_{L_n}.
- * Source: the KDA recurrence of the project's problem statement; the pages
+ * Source: Kimi Delta Attention, the gated delta rule with a per-channel decay
+ * gate (the pages name the method but print no formula); the pages
  * ("feat(kda/sm90): FlashKDA prefill port + intracard-CP prefill", commit
- * notes) fix CHUNK=16, D=128, forward only, and name the two stages
- * "K1 prepares decayed q/k, beta and the WY inverse; K2 runs the inter-chunk
- * recurrence", and the segment pipeline "K1 once -> pre_scan -> merge ->
- * segment-K2".
+ * notes) fix chunks of 16 tokens, head size 128 and the forward pass only;
+ * they split the work into K1 (decayed q/k, beta and the WY inverse per chunk)
+ * and K2 (the state carried from chunk to chunk), and the segment pipeline into
+ * K1 once, per-segment summaries (pre_scan), the merge, and K2 per segment.
  *
  * Three independent forms are provided:
  *   kda_oracle_recurrent  token by token, the formula written out (O1).

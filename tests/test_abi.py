@@ -152,6 +152,12 @@ def test_planner_decisions(lib):
     assert m == K.MODE_SEGMENT and s % 16 == 0
 
 
+def test_planner_picks_the_measured_best_segment_length(lib):
+    # T = 131072, H = 4 on GB300: segments of 512 / 1024 / 2048 / 4096 / 8192 / 16384
+    # tokens ran in 2.09 / 1.62 / 1.52 / 1.42 / 1.32 / 2.54 ms against 6.70 ms serial.
+    assert K.kda_plan(1, 131072, 4, 76) == (K.MODE_SEGMENT, 8192)
+
+
 @pytest.mark.parametrize("chains_per_cluster", [1, 2])
 @pytest.mark.parametrize("T", [16384, 131072, 1 << 20])
 def test_planner_keeps_serial_when_chains_fill_the_gpu(lib, chains_per_cluster, T):

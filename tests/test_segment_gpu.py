@@ -1,7 +1,8 @@
 """Segment-parallel prefill (pre_scan -> merge -> segment-K2) on the GPU.
 
 The pages claim the segment pipeline is bit-identical to the serial one (cuLA PR #103
-commit notes and test list: "CP vs serial bit-exactness (torch.equal)").  Under the
+commit notes and test list: a bit-exactness test of the context-parallel path against
+the serial path).  Under the
 plain reading of the pipeline the carries are products of per-segment transitions and
 round differently from the serial chain, so this suite requires both modes to match
 the fp64 oracle within atol = rtol = 1e-2 and reports the max abs difference between
