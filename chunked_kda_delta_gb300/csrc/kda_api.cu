@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -41,6 +42,7 @@ __device__ int32_t g_status_word = 0;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultWaitLimit = 1ll << 22;
 constexpr size_t kMaxWorkspaces = 8;
+constexpr int kMaxHostPieces = 64;  // pieces kda_prefill_host may stream a call in
 
 struct DeviceInfo {
     bool ready = false;
@@ -291,7 +293,9 @@ kda_status validate_options(const kda_options* o, const Problem& pr, int32_t* mo
     if (!o) return KDA_OK;
     if (o->debug_flags & ~KDA_DEBUG_STALL_WAIT)
         return fail(KDA_ERR_INVALID_ARGUMENT, "unknown debug_flags bits 0x%x", o->debug_flags);
-    if (o->reserved != 0) return fail(KDA_ERR_INVALID_ARGUMENT, "reserved must be 0");
+    if (o->host_pieces < 0 || o->host_pieces > kMaxHostPieces)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "host_pieces must be in [0, %d] (got %d)",
+                    kMaxHostPieces, o->host_pieces);
     *debug_flags = o->debug_flags;
     if (o->mode != KDA_MODE_SERIAL && o->mode != KDA_MODE_SEGMENT && o->mode != KDA_MODE_AUTO)
         return fail(KDA_ERR_INVALID_ARGUMENT, "unknown mode %d", o->mode);
@@ -604,6 +608,123 @@ kda_status kda_prefill(const kda_shape* shape, const uint16_t* q, const uint16_t
                           final_state, stream, nullptr);
 }
 
+// ---------------------------------------------------------------------------
+// kda_prefill_host streams the host buffers through the GPU in pieces: piece b's inputs
+// copy in on a copy-in stream while earlier pieces compute on the caller's stream and
+// their outputs copy out on a copy-out stream, so the host link carries both directions
+// at once and the kernels hide under the copies.  Several sequences split into ranges of
+// whole sequences (every chain computes exactly as in one call); one sequence splits into
+// token blocks of whole chunks, its fp32 state carried from block to block in place.
+constexpr int kAutoHostPieces = 8;
+constexpr size_t kHostPipelineMinBytes = (size_t)32 << 20;  // smaller inputs: one piece
+
+struct HostPipe {
+    int device = 0;
+    void* stream = nullptr;
+    cudaStream_t in = nullptr, out = nullptr;  // copy-in and copy-out streams
+    cudaEvent_t start = nullptr, out_done = nullptr;
+    cudaEvent_t in_done[kMaxHostPieces] = {}, computed[kMaxHostPieces] = {};
+    unsigned long long last_use = 0;
+};
+std::vector<std::unique_ptr<HostPipe>> g_pipes;  // per (device, caller stream), g_mutex
+
+void destroy_pipe(HostPipe& hp) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(hp.device);
+    for (cudaStream_t st : {hp.in, hp.out})
+        if (st) {
+            cudaStreamSynchronize(st);
+            cudaStreamDestroy(st);
+        }
+    for (cudaEvent_t ev : {hp.start, hp.out_done})
+        if (ev) cudaEventDestroy(ev);
+    for (int i = 0; i < kMaxHostPieces; ++i) {
+        if (hp.in_done[i]) cudaEventDestroy(hp.in_done[i]);
+        if (hp.computed[i]) cudaEventDestroy(hp.computed[i]);
+    }
+    cudaSetDevice(cur);
+}
+
+kda_status get_pipe(int dev, cudaStream_t stream, HostPipe** out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (auto& hp : g_pipes)
+        if (hp->device == dev && hp->stream == (void*)stream) {
+            hp->last_use = ++g_use_clock;
+            *out = hp.get();
+            return KDA_OK;
+        }
+    if (g_pipes.size() >= kMaxWorkspaces) {
+        size_t lru = 0;
+        for (size_t i = 1; i < g_pipes.size(); ++i)
+            if (g_pipes[i]->last_use < g_pipes[lru]->last_use) lru = i;
+        destroy_pipe(*g_pipes[lru]);
+        g_pipes.erase(g_pipes.begin() + lru);
+    }
+    auto hp = std::make_unique<HostPipe>();
+    hp->device = dev;
+    hp->stream = (void*)stream;
+    cudaError_t e;
+    const unsigned ef = cudaEventDisableTiming;
+    if ((e = cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking)) ||
+        (e = cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking)) ||
+        (e = cudaEventCreateWithFlags(&hp->start, ef)) ||
+        (e = cudaEventCreateWithFlags(&hp->out_done, ef))) {
+        destroy_pipe(*hp);
+        return cuda_fail(e, "copy stream / event creation");
+    }
+    for (int i = 0; i < kMaxHostPieces; ++i)
+        if ((e = cudaEventCreateWithFlags(&hp->in_done[i], ef)) ||
+            (e = cudaEventCreateWithFlags(&hp->computed[i], ef))) {
+            destroy_pipe(*hp);
+            return cuda_fail(e, "copy event creation");
+        }
+    hp->last_use = ++g_use_clock;
+    *out = hp.get();
+    g_pipes.push_back(std::move(hp));
+    return KDA_OK;
+}
+
+struct HostPiece {
+    int32_t n0, n1;  // sequences [n0, n1) (a token block: 0, 1)
+    int64_t t0, t1;  // tokens [t0, t1) of the flattened token axis
+};
+
+// At most `want` pieces of a problem: balanced ranges of whole sequences when there are
+// several, else token blocks of whole chunks of the one sequence (*blocks = true).
+std::vector<HostPiece> host_pieces(const Problem& pr, const int32_t* cu, int want, bool* blocks) {
+    std::vector<HostPiece> v;
+    *blocks = false;
+    auto start = [&](int32_t n) -> int64_t { return cu ? (int64_t)cu[n] : (int64_t)n * pr.dense_len; };
+    if (want <= 1 || pr.T_total == 0) {
+        v.push_back({0, pr.N, 0, pr.T_total});
+        return v;
+    }
+    if (pr.N >= 2) {
+        const int P = want < pr.N ? want : pr.N;
+        int32_t n0 = 0;
+        for (int b = 1; b <= P; ++b) {
+            int32_t n1 = pr.N;
+            if (b < P) {  // the first sequence end at or past b/P of the tokens, leaving
+                          // one sequence at least for every later piece
+                const int64_t target = pr.T_total * b / P;
+                n1 = n0 + 1;
+                while (n1 < pr.N - (P - b) && start(n1) < target) ++n1;
+            }
+            v.push_back({n0, n1, start(n0), start(n1)});
+            n0 = n1;
+        }
+        return v;
+    }
+    const int64_t nck = (pr.T_total + kda::kChunk - 1) / kda::kChunk;
+    const int64_t P = want < nck ? want : nck;
+    const int64_t per = (nck + P - 1) / P * kda::kChunk;
+    *blocks = true;
+    for (int64_t t0 = 0; t0 < pr.T_total; t0 += per)
+        v.push_back({0, 1, t0, t0 + per < pr.T_total ? t0 + per : pr.T_total});
+    return v;
+}
+
 kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
                             const uint16_t* v, const float* g, const uint16_t* beta,
                             float scale, const float* initial_state,
@@ -627,48 +748,137 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
             if (cu_seqlens[n + 1] < cu_seqlens[n])
                 return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must be non-decreasing");
     }
-    const Sizes sz = sizes_of(pr);
-    const size_t sb = sz.state;
-    const size_t cub = pr.varlen ? (size_t)(pr.N + 1) * 4 : 0;
-    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    const size_t off_q = 0, off_k = off_q + up(sz.q), off_v = off_k + up(sz.k),
-                 off_g = off_v + up(sz.v), off_b = off_g + up(sz.g), off_s0 = off_b + up(sz.beta),
-                 off_cu = off_s0 + (initial_state ? up(sb) : 0), off_out = off_cu + up(cub),
-                 off_fin = off_out + up(sz.out), total = off_fin + (final_state ? up(sb) : 0);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     DeviceInfo* di = nullptr;
     if ((st = device_info(dev, &di)) != KDA_OK) return st;
+    const Sizes sz = sizes_of(pr);
+    // Pieces: serial plans only (segment mode needs the whole sequence in one call).
+    int32_t plan_mode = mode, plan_len = 0;  // the whole problem's plan, AUTO resolved
+    if (mode == KDA_MODE_AUTO) choose_plan(pr, di->resident_clusters, &plan_mode, &plan_len);
+    const int32_t asked = opts ? opts->host_pieces : 0;
+    int want = 1;
+    if (plan_mode == KDA_MODE_SERIAL)
+        want = asked > 0 ? asked
+                         : (sz.q + sz.k + sz.v + sz.g + sz.beta >= kHostPipelineMinBytes ? kAutoHostPieces : 1);
+    bool blocks = false;
+    const std::vector<HostPiece> pieces = host_pieces(pr, cu_seqlens, want, &blocks);
+    const int P = (int)pieces.size();
+    const int32_t piece_mode = P > 1 ? plan_mode : mode;
+
+    // Device arena: the whole problem's tensors at their natural offsets, the offsets of
+    // every piece rebased to its first token, and one state table (final states, or the
+    // state carried between token blocks).
+    const size_t sb = sz.state;
+    const bool need_fin = final_state != nullptr || blocks;
+    const size_t cub = pr.varlen ? (size_t)(pr.N + P) * 4 : 0;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t off_q = 0, off_k = off_q + up(sz.q), off_v = off_k + up(sz.k),
+                 off_g = off_v + up(sz.v), off_b = off_g + up(sz.g), off_s0 = off_b + up(sz.beta),
+                 off_cu = off_s0 + (initial_state ? up(sb) : 0), off_out = off_cu + up(cub),
+                 off_fin = off_out + up(sz.out), total = off_fin + (need_fin ? up(sb) : 0);
     void* base = nullptr;
-    if ((st = get_workspace(dev, stream, kWsHostArena, total, &base)) != KDA_OK)
-        return st;
+    if ((st = get_workspace(dev, stream, kWsHostArena, total, &base)) != KDA_OK) return st;
+    HostPipe* hp = nullptr;
+    if ((st = get_pipe(dev, stream, &hp)) != KDA_OK) return st;
     char* b = static_cast<char*>(base);
-    struct Cp {
-        void* dst;
-        const void* src;
-        size_t n;
-    } ins[] = {{b + off_q, q, sz.q},  {b + off_k, k, sz.k},  {b + off_v, v, sz.v},
-               {b + off_g, g, sz.g},  {b + off_b, beta, sz.beta},
-               {b + off_s0, initial_state, initial_state ? sb : 0},
-               {b + off_cu, cu_seqlens, cub}};
-    for (auto& c : ins)
-        if (c.n && (e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, stream)))
-            return cuda_fail(e, "cudaMemcpyAsync host->device");
+    uint16_t* d_q = reinterpret_cast<uint16_t*>(b + off_q);
+    uint16_t* d_k = reinterpret_cast<uint16_t*>(b + off_k);
+    uint16_t* d_v = reinterpret_cast<uint16_t*>(b + off_v);
+    float* d_g = reinterpret_cast<float*>(b + off_g);
+    uint16_t* d_beta = reinterpret_cast<uint16_t*>(b + off_b);
+    float* d_s0 = initial_state ? reinterpret_cast<float*>(b + off_s0) : nullptr;
+    int32_t* d_cu = reinterpret_cast<int32_t*>(b + off_cu);
     uint16_t* d_out = reinterpret_cast<uint16_t*>(b + off_out);
-    float* d_fin = final_state ? reinterpret_cast<float*>(b + off_fin) : nullptr;
-    st = run(pr, reinterpret_cast<uint16_t*>(b + off_q), reinterpret_cast<uint16_t*>(b + off_k),
-             reinterpret_cast<uint16_t*>(b + off_v), reinterpret_cast<float*>(b + off_g),
-             reinterpret_cast<uint16_t*>(b + off_b),
-             scale, initial_state ? reinterpret_cast<float*>(b + off_s0) : nullptr,
-             pr.varlen ? reinterpret_cast<int32_t*>(b + off_cu) : nullptr, d_out, d_fin, stream,
-             mode, seg_len, wait_limit, debug_flags);
-    if (st != KDA_OK) return st;
-    if (sz.out && (e = cudaMemcpyAsync(out, d_out, sz.out, cudaMemcpyDeviceToHost, stream)))
-        return cuda_fail(e, "cudaMemcpyAsync device->host (out)");
-    if (d_fin && (e = cudaMemcpyAsync(final_state, d_fin, sb, cudaMemcpyDeviceToHost, stream)))
-        return cuda_fail(e, "cudaMemcpyAsync device->host (final_state)");
-    if ((e = cudaStreamSynchronize(stream))) return cuda_fail(e, "cudaStreamSynchronize");
+    float* d_fin = need_fin ? reinterpret_cast<float*>(b + off_fin) : nullptr;
+    const size_t D = kda::kD, st_elems = (size_t)pr.H * D * D;  // one sequence's states
+    std::vector<int32_t> cu_rebased;
+    std::vector<size_t> cu_at(P, 0);
+    if (pr.varlen) {
+        cu_rebased.reserve((size_t)pr.N + P);
+        for (int i = 0; i < P; ++i) {
+            cu_at[i] = cu_rebased.size();
+            for (int32_t n = pieces[i].n0; n <= pieces[i].n1; ++n)
+                cu_rebased.push_back(cu_seqlens[n] - cu_seqlens[pieces[i].n0]);
+        }
+    }
+
+    // Every error after the first copy is queued waits for all three streams, so no copy
+    // touches the caller's buffers after the call returns.
+    auto drain = [&](kda_status s) {
+        cudaStreamSynchronize(hp->in);
+        cudaStreamSynchronize(hp->out);
+        cudaStreamSynchronize(stream);
+        return s;
+    };
+    if ((e = cudaEventRecord(hp->start, stream)) || (e = cudaStreamWaitEvent(hp->in, hp->start, 0)))
+        return cuda_fail(e, "copy-in ordering");
+    auto h2d = [&](void* dst, const void* src, size_t n) {
+        return n ? cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, hp->in) : cudaSuccess;
+    };
+    if (pr.varlen && (e = h2d(d_cu, cu_rebased.data(), cu_rebased.size() * 4)))
+        return drain(cuda_fail(e, "cudaMemcpyAsync host->device (cu_seqlens)"));
+    for (int i = 0; i < P; ++i) {
+        const HostPiece& pc = pieces[i];
+        const size_t t0 = (size_t)pc.t0, nt = (size_t)(pc.t1 - pc.t0);
+        const size_t tq = (size_t)pr.Hq * D, tk = (size_t)pr.Hk * D, tv = (size_t)pr.H * D;
+        const size_t s_first = blocks ? 0 : (size_t)pc.n0, s_count = blocks ? (i == 0 ? 1 : 0)
+                                                                             : (size_t)(pc.n1 - pc.n0);
+        if ((e = h2d(d_q + t0 * tq, q + t0 * tq, nt * tq * 2)) ||
+            (e = h2d(d_k + t0 * tk, k + t0 * tk, nt * tk * 2)) ||
+            (e = h2d(d_v + t0 * tv, v + t0 * tv, nt * tv * 2)) ||
+            (e = h2d(d_g + t0 * tv, g + t0 * tv, nt * tv * 4)) ||
+            (e = h2d(d_beta + t0 * pr.H, beta + t0 * pr.H, nt * pr.H * 2)) ||
+            (initial_state && (e = h2d(d_s0 + s_first * st_elems, initial_state + s_first * st_elems,
+                                       s_count * st_elems * 4))) ||
+            (e = cudaEventRecord(hp->in_done[i], hp->in)))
+            return drain(cuda_fail(e, "cudaMemcpyAsync host->device"));
+    }
+    // Compute every piece on the caller's stream, each after its own copy-in.
+    for (int i = 0; i < P; ++i) {
+        const HostPiece& pc = pieces[i];
+        Problem pp = pr;
+        pp.T_total = pc.t1 - pc.t0;
+        if (blocks) {
+            pp.N = 1;
+            pp.varlen = false;
+            pp.dense_len = pp.T_total;
+        } else {
+            pp.N = pc.n1 - pc.n0;
+        }
+        const size_t t0 = (size_t)pc.t0, n0 = blocks ? 0 : (size_t)pc.n0;
+        const float* s0 = blocks ? (i == 0 ? d_s0 : d_fin) : (d_s0 ? d_s0 + n0 * st_elems : nullptr);
+        float* sfin = d_fin ? d_fin + n0 * st_elems : nullptr;
+        if ((e = cudaStreamWaitEvent(stream, hp->in_done[i], 0)))
+            return drain(cuda_fail(e, "cudaStreamWaitEvent"));
+        st = run(pp, d_q + t0 * pr.Hq * D, d_k + t0 * pr.Hk * D, d_v + t0 * pr.H * D,
+                 d_g + t0 * pr.H * D, d_beta + t0 * pr.H, scale, s0,
+                 pr.varlen ? d_cu + cu_at[i] : nullptr, d_out + t0 * pr.Ho * D, sfin, stream,
+                 piece_mode, seg_len, wait_limit, debug_flags);
+        if (st != KDA_OK) return drain(st);
+        if ((e = cudaEventRecord(hp->computed[i], stream)))
+            return drain(cuda_fail(e, "cudaEventRecord"));
+    }
+    // Copy out each piece once it has computed (final states of whole sequences with their
+    // piece; a carried state after the last block).
+    for (int i = 0; i < P; ++i) {
+        const HostPiece& pc = pieces[i];
+        const size_t t0 = (size_t)pc.t0, nt = (size_t)(pc.t1 - pc.t0), to = (size_t)pr.Ho * D;
+        if ((e = cudaStreamWaitEvent(hp->out, hp->computed[i], 0)))
+            return drain(cuda_fail(e, "cudaStreamWaitEvent"));
+        if (nt && (e = cudaMemcpyAsync(out + t0 * to, d_out + t0 * to, nt * to * 2,
+                                       cudaMemcpyDeviceToHost, hp->out)))
+            return drain(cuda_fail(e, "cudaMemcpyAsync device->host (out)"));
+        const bool fin_now = final_state && (blocks ? i == P - 1 : pc.n1 > pc.n0);
+        const size_t n0 = blocks ? 0 : (size_t)pc.n0, nn = blocks ? 1 : (size_t)(pc.n1 - pc.n0);
+        if (fin_now && (e = cudaMemcpyAsync(final_state + n0 * st_elems, d_fin + n0 * st_elems,
+                                            nn * st_elems * 4, cudaMemcpyDeviceToHost, hp->out)))
+            return drain(cuda_fail(e, "cudaMemcpyAsync device->host (final_state)"));
+    }
+    if ((e = cudaEventRecord(hp->out_done, hp->out)) || (e = cudaStreamWaitEvent(stream, hp->out_done, 0)))
+        return drain(cuda_fail(e, "copy-out ordering"));
+    if ((e = cudaStreamSynchronize(stream))) return drain(cuda_fail(e, "cudaStreamSynchronize"));
     return KDA_OK;
 }
 
@@ -781,6 +991,14 @@ kda_status kda_release_workspaces(int32_t device) {
             cudaDeviceSynchronize();
             cudaFree(g_workspaces[i].ptr);
             g_workspaces.erase(g_workspaces.begin() + i);
+        } else {
+            ++i;
+        }
+    }
+    for (size_t i = 0; i < g_pipes.size();) {
+        if (device < 0 || g_pipes[i]->device == device) {
+            destroy_pipe(*g_pipes[i]);
+            g_pipes.erase(g_pipes.begin() + i);
         } else {
             ++i;
         }

@@ -56,7 +56,7 @@ class KdaShape(ctypes.Structure):
 class KdaOptions(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("segment_len", ctypes.c_int32),
                 ("wait_limit", ctypes.c_int64), ("debug_flags", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("host_pieces", ctypes.c_int32)]
 
 
 _lib = None
@@ -190,8 +190,9 @@ def _check_result(name, t, shape, dtype, device_type):
 DEBUG_STALL_WAIT = 1
 
 
-def _options(mode, segment_len, wait_limit, debug_flags=0):
-    return KdaOptions(int(mode), int(segment_len), int(wait_limit), int(debug_flags), 0)
+def _options(mode, segment_len, wait_limit, debug_flags=0, host_pieces=0):
+    return KdaOptions(int(mode), int(segment_len), int(wait_limit), int(debug_flags),
+                      int(host_pieces))
 
 
 def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
@@ -249,11 +250,14 @@ def kda_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
                      out: Optional[torch.Tensor] = None,
                      final_state: Optional[torch.Tensor] = None,
                      stream=None, output_final_state: bool = False, device=None,
-                     mode: int = MODE_SERIAL, segment_len: int = 0, wait_limit: int = 0):
+                     mode: int = MODE_SERIAL, segment_len: int = 0, wait_limit: int = 0,
+                     host_pieces: int = 0):
     """End-to-end prefill on HOST (CPU) tensors: copy in, compute, copy out, synchronise.
 
     Same arguments as :func:`kda_prefill` but every tensor lives in host memory
-    (pinned memory gives full copy bandwidth); ``device`` picks the GPU.
+    (pinned memory gives full copy bandwidth); ``device`` picks the GPU.  Large serial
+    calls stream in ``host_pieces`` pieces (0: the library's choice) so that copies
+    and kernels overlap.
     """
     lib = load_library()
     _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, "cpu")
@@ -274,7 +278,7 @@ def kda_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
         stream = torch.cuda.current_stream(dev).cuda_stream
     elif isinstance(stream, torch.cuda.Stream):
         stream = stream.cuda_stream
-    opts = _options(mode, segment_len, wait_limit)
+    opts = _options(mode, segment_len, wait_limit, host_pieces=host_pieces)
     with torch.cuda.device(dev):
         st = lib.kda_prefill_host(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                   _ptr(beta), ctypes.c_float(scale), _ptr(initial_state),

@@ -102,7 +102,9 @@ typedef struct kda_options {
     int32_t segment_len;  /* segment mode: tokens per segment, multiple of 16; 0 = 8192 */
     int64_t wait_limit;   /* iteration limit of each device spin wait; 0 = library default */
     int32_t debug_flags;  /* 0 in normal use; KDA_DEBUG_* bits for failure-path tests */
-    int32_t reserved;     /* must be 0 */
+    int32_t host_pieces;  /* kda_prefill_host: pieces the call is streamed in, 0..64;
+                             0 = the library's choice, 1 = one piece; ignored by the
+                             device entry points */
 } kda_options;
 
 /* debug_flags bit: the kernel's first state-pipeline wait is on a barrier that nothing
@@ -141,10 +143,22 @@ kda_status kda_prefill_ex(const kda_shape* shape, const uint16_t* q, const uint1
 /* kda_prefill_host -- the same computation on HOST buffers, end to end.
  * Every tensor pointer (including cu_seqlens) is a host pointer with the
  * layouts above; page-locked memory gives full copy bandwidth.  The call
- * copies the inputs into a library-owned device arena on `stream`, runs the
- * prefill, copies out (and final_state when non-NULL) back, and synchronises
- * `stream` before returning.  The arena is kept per (device, stream) and
- * reused; it is freed by kda_release_workspaces(). */
+ * copies the inputs into a library-owned device arena, runs the prefill on
+ * `stream`, copies out (and final_state when non-NULL) back, and synchronises
+ * `stream` before returning.
+ *   Streaming: in serial mode (chosen, or picked by KDA_MODE_AUTO) a call whose
+ *   inputs reach 32 MiB runs in pieces (8 by default, opts->host_pieces to set):
+ *   each piece's inputs copy in on a library stream while earlier pieces compute
+ *   on `stream` and their outputs copy out on a second library stream, so input
+ *   copies, output copies and kernels overlap.  Several sequences split into
+ *   ranges of whole sequences, balanced by tokens: the results are bit-identical
+ *   to one kda_prefill_ex call.  One sequence splits into token blocks of whole
+ *   16-token chunks, the fp32 state carried from block to block in the arena:
+ *   the results equal one call up to rounding (each block restarts the chunk
+ *   pipeline from the stored state).  Segment mode runs in one piece.
+ *   Both copy streams, their events and the arena are kept per (device, stream)
+ *   and reused; kda_release_workspaces() frees them.  Concurrent calls with the
+ *   same stream from several threads are not supported. */
 kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
                             const uint16_t* v, const float* g, const uint16_t* beta,
                             float scale, const float* initial_state,

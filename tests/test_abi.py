@@ -96,7 +96,10 @@ def test_options_rules(lib):
     assert _call(lib, s, opts=KdaOptions(1, -16, 0, 0, 0)) == INVALID
     assert _call(lib, s, opts=KdaOptions(0, 0, -1, 0, 0)) == INVALID
     assert _call(lib, s, opts=KdaOptions(0, 0, 0, 2, 0)) == INVALID    # unknown debug bit
-    assert _call(lib, s, opts=KdaOptions(0, 0, 0, 0, 1)) == INVALID    # reserved != 0
+    assert _call(lib, s, opts=KdaOptions(0, 0, 0, 0, -1)) == INVALID   # host_pieces < 0
+    assert _call(lib, s, opts=KdaOptions(0, 0, 0, 0, 65)) == INVALID   # host_pieces > 64
+    # host_pieces is a host-entry setting; the device entry points accept and ignore it
+    assert _call(lib, s, opts=KdaOptions(0, 0, 0, 0, 8)) not in (INVALID, ALIAS)
 
 
 def test_aliasing_rules(lib):
