@@ -375,6 +375,7 @@ struct SegPlan {
 constexpr double kMergePerSegment = 5.0;
 constexpr double kSegmentMargin = 0.8;      // segment mode must win by 20%
 constexpr size_t kPlanWorkspaceCap = (size_t)4 << 30;
+constexpr int64_t kMinPlanSegment = 512;  // shortest segment the planner considers
 
 void choose_plan(const Problem& pr, int64_t resident, int32_t* mode, int32_t* seg_len) {
     *mode = KDA_MODE_SERIAL;
@@ -389,11 +390,18 @@ void choose_plan(const Problem& pr, int64_t resident, int32_t* mode, int32_t* se
     const double serial = (double)cdiv(Co, R) * (double)nck;
     double best = serial;
     int32_t best_len = 0;
-    for (int64_t sl = 512; sl <= ((int64_t)1 << 20); sl *= 2) {
+    // Candidates: for each segment count n, the shortest multiple of 16 tokens that covers
+    // the sequence in n segments.  These include every count whose passes fill the cluster
+    // slots exactly (C n = R for few chains), which lengths on a power-of-two grid miss.
+    int64_t prev = -1;
+    for (int64_t n = 2;; ++n) {
+        const int64_t sl = cdiv(cdiv(pr.dense_len, n), kda::kChunk) * kda::kChunk;
+        if (sl < kMinPlanSegment) break;
+        if (sl == prev || sl > ((int64_t)1 << 30)) continue;
+        prev = sl;
         const int64_t nseg = cdiv(pr.dense_len, sl);
-        if (nseg < 2) break;
         const size_t ws = (size_t)(3 * nseg - 2) * (size_t)C * kda::kD * kda::kD * 4;
-        if (ws > kPlanWorkspaceCap) continue;
+        if (ws > kPlanWorkspaceCap) break;  // grows with n
         const double waves = (double)(2 * cdiv(C * (nseg - 1), R) + cdiv(Co * nseg, R));
         const double cost = waves * (double)(sl / kda::kChunk) + kMergePerSegment * (double)nseg;
         if (cost < best) {

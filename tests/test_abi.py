@@ -156,9 +156,15 @@ def test_planner_decisions(lib):
 
 
 def test_planner_picks_the_measured_best_segment_length(lib):
-    # T = 131072, H = 4 on GB300: segments of 512 / 1024 / 2048 / 4096 / 8192 / 16384
-    # tokens ran in 2.09 / 1.62 / 1.52 / 1.42 / 1.32 / 2.54 ms against 6.70 ms serial.
-    assert K.kda_plan(1, 131072, 4, 76) == (K.MODE_SEGMENT, 8192)
+    # T = 131072 on GB300 (L2 flushed before each call), segment mode:
+    #   H = 4: 8192 / 7296 / 6912 / 6560 tokens (16 / 18 / 19 / 20 segments) took
+    #          1.40 / 1.27 / 1.20 / 1.47 ms (serial 7.13 ms); 19 segments fill the 76
+    #          cluster slots in every pass;
+    #   H = 2: 4096 / 3456 tokens 0.740 / 0.664 ms;  H = 8: 2048 / 3456 / 6912 tokens
+    #          2.52 / 2.31 / 2.21 ms.
+    assert K.kda_plan(1, 131072, 4, 76) == (K.MODE_SEGMENT, 6912)
+    assert K.kda_plan(1, 131072, 2, 76) == (K.MODE_SEGMENT, 3456)
+    assert K.kda_plan(1, 131072, 8, 76) == (K.MODE_SEGMENT, 6912)
 
 
 @pytest.mark.parametrize("chains_per_cluster", [1, 2])
