@@ -261,6 +261,17 @@ def test_grouped_planner(lib):
     assert nb == (3 * 4 - 2) * 2 * 128 * 128 * 4
 
 
+def test_host_pieces_range_checked_before_device_work(lib):
+    # the host entry validates its options before it touches a device or a buffer
+    s = KdaShape(1, 16, 0, 2, 128)
+    P = ctypes.c_void_p
+    for bad in (-1, 65):
+        st = lib.kda_prefill_host(ctypes.byref(s), P(0x1000), P(0x2000), P(0x3000), P(0x4000),
+                                  P(0x5000), ctypes.c_float(0.1), None, None, P(0x6000), None,
+                                  None, ctypes.byref(KdaOptions(0, 0, 0, 0, bad)))
+        assert st == INVALID and b"host_pieces" in lib.kda_last_error_message()
+
+
 def test_binding_refuses_short_outputs():
     # a caller-supplied output smaller than what the library writes is refused before the
     # call (the ABI sees only a pointer); here q has 2 heads and v 6, so out has 6
