@@ -11,27 +11,31 @@
 // independent, so each CTA runs the whole serial chain over segments for its block.  The
 // next segment's transition and summary block stream into a second shared-memory buffer
 // (16-byte cp.async) while the current product runs, so a step of the chain waits on no
-// global load.  The block width is the widest of 32 / 16 / 8 columns that still gives
-// every SM a CTA, so that few heads spread over the GPU.
+// global load.  The two halves of the CTA take the two halves of each product's K range
+// (the upper half hands its partial sums over in shared memory), so sixteen warps hide
+// the shared-memory load latency of a step.  The block width is the widest of 32 / 16 /
+// 8 columns that still gives every SM a CTA, so that few heads spread over the GPU.
 // fp32 throughout (the carries feed every later output of their segment).
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 512;              // two K halves of 256 threads
+constexpr int kHalfThreads = kMergeThreads / 2;
 constexpr int kMRow = kD + 4;  // padded row of a transition in shared memory
 
 template <int kCols>
 struct MergeShape {
-    static constexpr int kColGroups = kCols / 4;                   // float4 columns
-    static constexpr int kRowGroups = kMergeThreads / kColGroups;  // threads along rows
-    static constexpr int kRowsPer = kD / kRowGroups;               // rows per thread
-    static constexpr int kBRow = kCols + 4;                        // padded row of a block
+    static constexpr int kColGroups = kCols / 4;                  // float4 columns
+    static constexpr int kRowGroups = kHalfThreads / kColGroups;  // threads along rows
+    static constexpr int kRowsPer = kD / kRowGroups;              // rows per thread
+    static constexpr int kBRow = kCols + 4;                       // padded row of a block
     static constexpr int kMFloats = kD * kMRow;
     static constexpr int kBFloats = kD * kBRow;
-    // two transitions, two summary blocks, the carry block
-    static constexpr int kSmem = (2 * kMFloats + 3 * kBFloats) * 4;
+    static constexpr int kPFloats = kHalfThreads * kRowsPer * 4;  // upper-half partials
+    // two transitions, two summary blocks, the carry block, the partials
+    static constexpr int kSmem = (2 * kMFloats + 3 * kBFloats + kPFloats) * 4;
 };
 
 __device__ __forceinline__ void cp_async16(float* sdst, const float* gsrc) {
@@ -54,7 +58,9 @@ kda_merge_kernel(const float* __restrict__ m_seg, const float* __restrict__ b_se
     float* Ms = sm;                        // two transitions m[i][k], rows padded
     float* Bsm = sm + 2 * S::kMFloats;     // two summary blocks b[i][c]
     float* Cb = Bsm + 2 * S::kBFloats;     // carry block [k][c]
+    float* Pp = Cb + S::kBFloats;          // partial sums of the upper K half
     const int tid = threadIdx.x;
+    const int lo = tid % kHalfThreads, kh = tid / kHalfThreads;  // K half: keys 64 kh ..
     constexpr int kBlocks = kD / kCols;
     const int cb = blockIdx.x % kBlocks;
     const int h = (blockIdx.x / kBlocks) % H;
@@ -62,8 +68,8 @@ kda_merge_kernel(const float* __restrict__ m_seg, const float* __restrict__ b_se
     // Thread tile: rows rg + kRowGroups*a (a < kRowsPer), columns c0..c0+3 of the block.
     // A warp's rows are consecutive, so its float4 reads of a padded transition row fall
     // on distinct banks; its columns are consecutive float4s of one carry row.
-    const int rg = tid / S::kColGroups;
-    const int c0 = (tid % S::kColGroups) * 4;
+    const int rg = lo / S::kColGroups;
+    const int c0 = (lo % S::kColGroups) * 4;
     const size_t st = (size_t)kD * kD;
     // Dense: summaries [B][nseg-1][H], carries [B][nseg][H].  Varlen: every table indexed
     // by the global segment row g = seg_start[b] + s, sequence b owning its own count.
@@ -118,14 +124,15 @@ kda_merge_kernel(const float* __restrict__ m_seg, const float* __restrict__ b_se
         float acc[S::kRowsPer][4];
 #pragma unroll
         for (int a = 0; a < S::kRowsPer; ++a) {
-            const float4 bv = *reinterpret_cast<const float4*>(Bb + (rg + S::kRowGroups * a) * S::kBRow + c0);
+            float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (kh == 0) bv = *reinterpret_cast<const float4*>(Bb + (rg + S::kRowGroups * a) * S::kBRow + c0);
             acc[a][0] = bv.x;
             acc[a][1] = bv.y;
             acc[a][2] = bv.z;
             acc[a][3] = bv.w;
         }
 #pragma unroll 2
-        for (int k = 0; k < kD; k += 4) {
+        for (int k = kh * (kD / 2); k < (kh + 1) * (kD / 2); k += 4) {
             float mm[S::kRowsPer][4];
 #pragma unroll
             for (int a = 0; a < S::kRowsPer; ++a) {
@@ -147,14 +154,24 @@ kda_merge_kernel(const float* __restrict__ m_seg, const float* __restrict__ b_se
                 }
             }
         }
-        __syncthreads();  // every read of the carry block and of buffer s&1 is done
-        float* out = carry_at(s + 1);
+        if (kh == 1) {
 #pragma unroll
-        for (int a = 0; a < S::kRowsPer; ++a) {
-            const int i = rg + S::kRowGroups * a;
-            const float4 o = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-            *reinterpret_cast<float4*>(Cb + i * S::kBRow + c0) = o;
-            *reinterpret_cast<float4*>(out + (size_t)i * kD + cb * kCols + c0) = o;
+            for (int a = 0; a < S::kRowsPer; ++a)
+                *reinterpret_cast<float4*>(Pp + (a * kHalfThreads + lo) * 4) =
+                    make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        }
+        __syncthreads();  // partials written; every read of the carry block and buffer s&1 done
+        if (kh == 0) {
+            float* out = carry_at(s + 1);
+#pragma unroll
+            for (int a = 0; a < S::kRowsPer; ++a) {
+                const int i = rg + S::kRowGroups * a;
+                const float4 pv = *reinterpret_cast<const float4*>(Pp + (a * kHalfThreads + lo) * 4);
+                const float4 o = make_float4(acc[a][0] + pv.x, acc[a][1] + pv.y, acc[a][2] + pv.z,
+                                             acc[a][3] + pv.w);
+                *reinterpret_cast<float4*>(Cb + i * S::kBRow + c0) = o;
+                *reinterpret_cast<float4*>(out + (size_t)i * kD + cb * kCols + c0) = o;
+            }
         }
     }
 }
