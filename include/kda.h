@@ -229,8 +229,10 @@ kda_status kda_decode(const kda_shape* shape, const uint16_t* q, const uint16_t*
 
 /* Bytes of device workspace a call with this shape and these options uses
  * (0 for serial mode).  A shape with num_seqs > 0 is taken as packed varlen input
- * (segment mode then sizes for at most num_seqs + seq_len / segment_len segments).  No device work, except that KDA_MODE_AUTO reads the current
- * device's resident cluster count to resolve the plan; *bytes is written on success. */
+ * (segment mode then sizes for at most num_seqs + seq_len / segment_len segments).
+ * kda_prefill_host holds, besides, an arena the size of its tensors.  No device work,
+ * except that KDA_MODE_AUTO reads the current device's resident cluster count to
+ * resolve the plan; *bytes is written on success. */
 kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, size_t* bytes);
 
 /* The execution plan KDA_MODE_AUTO picks for this shape on a device that holds
@@ -241,7 +243,10 @@ kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, 
  * state chain: every pass of the fused kernel costs about the same per chunk,
  * clusters beyond the resident count run in further waves, and the merge walks a
  * chain's segments in order (segment-parallel prefill, cuLA PR #103 "intracard-CP
- * prefill", planner notes).  Host only, no device work.  Errors:
+ * prefill", planner notes).  Candidates: for every segment count, the shortest
+ * multiple of 16 tokens (at least 512) that covers the sequence in that many
+ * segments, under a 4 GiB workspace cap; segment mode is chosen only when it beats
+ * serial by 20%.  Host only, no device work.  Errors:
  * KDA_ERR_INVALID_ARGUMENT for a bad shape, NULL outputs or resident_clusters < 1. */
 kda_status kda_plan(const kda_shape* shape, int32_t varlen, int32_t resident_clusters, int32_t* mode,
                     int32_t* segment_len);
