@@ -167,6 +167,32 @@ def test_planner_picks_the_measured_best_segment_length(lib):
     assert K.kda_plan(1, 131072, 8, 76) == (K.MODE_SEGMENT, 6912)
 
 
+def test_planner_choices_are_valid_plans(lib):
+    # Over a grid of dense shapes: a segment plan has a length that is a multiple of 16
+    # of at least 512 tokens, two segments or more, and a workspace (three state tables
+    # per segment and state head, less two) under the 4 GiB cap that kda_workspace_bytes
+    # reports for that length; chains that fill the 76 cluster slots stay serial.
+    import time
+    R = 76
+    for B in (1, 2):
+        for H in (1, 2, 3, 4, 8, 12, 16, 64, 128):
+            for T in (512, 1000, 4096, 32768, 131072, 1 << 20, 1 << 24):
+                m, sl = K.kda_plan(B, T, H, R)
+                if B * H >= R:
+                    assert (m, sl) == (K.MODE_SERIAL, 0), (B, H, T)
+                if m == K.MODE_SERIAL:
+                    assert sl == 0
+                    continue
+                nseg = -(-T // sl)
+                ws = (3 * nseg - 2) * B * H * 128 * 128 * 4
+                assert sl % 16 == 0 and sl >= 512 and nseg >= 2 and ws <= 4 << 30, (B, H, T, sl)
+                assert K.kda_workspace_bytes(B, T, H, mode=K.MODE_SEGMENT, segment_len=sl) == ws
+    # the candidate search stays cheap at the largest sequence the shape check allows
+    t0 = time.perf_counter()
+    K.kda_plan(1, 1 << 39, 1, R)
+    assert time.perf_counter() - t0 < 0.5
+
+
 @pytest.mark.parametrize("chains_per_cluster", [1, 2])
 @pytest.mark.parametrize("T", [16384, 131072, 1 << 20])
 def test_planner_keeps_serial_when_chains_fill_the_gpu(lib, chains_per_cluster, T):
