@@ -66,6 +66,15 @@ def test_sequence_ranges_bit_identical_packed(pieces):
     assert torch.equal(o_h, o_dev) and torch.equal(f_h, f_dev)
 
 
+@pytest.mark.parametrize("H,Hq", [(4, 8), (6, 2)])
+def test_sequence_ranges_bit_identical_grouped(H, Hq):
+    inp = make_inputs(custom([200, 0, 333, 64, 17], H, True, seed=3108 + Hq, dense=False,
+                             num_q_heads=Hq), DEV)
+    o_dev, f_dev = device_call(inp)
+    o_h, f_h = host_call(inp, 3)
+    assert torch.equal(o_h, o_dev) and torch.equal(f_h, f_dev)
+
+
 @pytest.mark.parametrize("pieces", [2, 5])
 def test_sequence_ranges_bit_identical_dense(pieces):
     inp = make_inputs(custom([200] * 5, 2, True, seed=3102, dense=True), DEV)
