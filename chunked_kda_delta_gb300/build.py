@@ -10,7 +10,9 @@ from __future__ import annotations
 
 import concurrent.futures
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -21,6 +23,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libkda.so")
+STAMP_PATH = LIB_PATH + ".stamp"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,22 +47,43 @@ def _deps():
         os.path.join(INCLUDE, "kda.h"), os.path.abspath(__file__)]
 
 
-def _up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stamp(flags) -> str:
+    """Digest of everything the library is built from: the source and header bytes,
+    the compiler flags, the host architecture and the nvcc version line.  A library
+    whose stamp differs (other sources, flags, or a library built on another machine
+    and copied here) is rebuilt."""
+    h = hashlib.sha256()
+    for d in _deps():
+        h.update(os.path.basename(d).encode())
+        with open(d, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(flags).encode())
+    h.update(platform.machine().encode())
+    try:
+        ver = subprocess.run([nvcc_path(), "--version"], capture_output=True, text=True).stdout
+    except (OSError, RuntimeError):
+        ver = ""
+    h.update(ver.encode())
+    return h.hexdigest()
+
+
+def _up_to_date(stamp: str) -> bool:
+    if not (os.path.exists(LIB_PATH) and os.path.exists(STAMP_PATH)):
         return False
-    t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(d) <= t for d in _deps())
+    with open(STAMP_PATH) as f:
+        return f.read().strip() == stamp
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile every CUDA source and link ``libkda.so``; returns the library path."""
-    if not force and _up_to_date():
-        return LIB_PATH
-    nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                     "--expt-relaxed-constexpr",
                     "-I", INCLUDE, "-I", CSRC, "-DKDA_BUILDING_LIBRARY"] + list(extra_flags)
+    stamp = _stamp(flags)
+    if not force and _up_to_date(stamp):
+        return LIB_PATH
+    nvcc = nvcc_path()
+    os.makedirs(BUILD_DIR, exist_ok=True)
     if verbose:
         flags += ["-Xptxas", "-v"]
 
@@ -86,6 +110,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
     os.replace(tmp, LIB_PATH)
+    with open(STAMP_PATH, "w") as f:
+        f.write(stamp + "\n")
     return LIB_PATH
 
 

@@ -456,6 +456,84 @@ SegPlan plan_segments(const Problem& pr, int32_t seg_len) {
     return sp;
 }
 
+// Kernel parameters of one call (pointers, sizes, wait limit, status word) and the TMA
+// descriptors of its tensors; shared by every entry point that launches the prefill.
+kda_status prepare_call(const Problem& pr, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const float* g, const uint16_t* beta, float scale, const float* s0,
+                        const int32_t* cu, uint16_t* out, float* sfin, int64_t wait_limit,
+                        int32_t debug_flags, int32_t* status, kda::FwdParams* p,
+                        kda::TensorMaps* maps) {
+    *p = kda::FwdParams{};
+    p->q = reinterpret_cast<const __nv_bfloat16*>(q);
+    p->k = reinterpret_cast<const __nv_bfloat16*>(k);
+    p->v = reinterpret_cast<const __nv_bfloat16*>(v);
+    p->g = g;
+    p->beta = reinterpret_cast<const __nv_bfloat16*>(beta);
+    p->s0 = s0;
+    p->sfin = sfin;
+    p->out = reinterpret_cast<__nv_bfloat16*>(out);
+    p->cu = cu;
+    p->T_total = pr.T_total;
+    p->dense_len = pr.dense_len;
+    p->N = pr.N;
+    p->H = pr.H;
+    p->Hq = pr.Hq;
+    p->scale = scale;
+    p->wait_limit = wait_limit;
+    p->debug_flags = debug_flags;
+    p->status = status;
+    memset(maps, 0, sizeof(*maps));
+    kda_status st = KDA_OK;
+    if (pr.T_total > 0) {
+        if ((st = encode_chunk_map(&maps->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hq, "q")) ||
+            (st = encode_chunk_map(&maps->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hk, "k")) ||
+            (st = encode_chunk_map(&maps->v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "v")) ||
+            (st = encode_chunk_map(&maps->g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")) ||
+            (st = encode_chunk_map(&maps->out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Ho, "out")))
+            return st;
+    }
+    return KDA_OK;
+}
+
+// Dense segment-parallel prefill on scratch `base` laid out by `sp` (sp.nseg >= 2):
+// pre_scan (segment summaries from zero and transitions from the identity, all segments
+// but the last, in parallel) -> merge (carries from the initial state) -> segment-K2.
+// Every scratch byte it reads is written earlier in the same call.
+kda_status run_dense_segments(const Problem& pr, const kda::FwdParams& p, const kda::TensorMaps& maps,
+                              const SegPlan& sp, int32_t seg_len, void* base, int sm_count,
+                              cudaStream_t stream) {
+    cudaError_t e;
+    float* b_seg = reinterpret_cast<float*>(static_cast<char*>(base) + sp.off_b);
+    float* m_seg = reinterpret_cast<float*>(static_cast<char*>(base) + sp.off_m);
+    float* carries = reinterpret_cast<float*>(static_cast<char*>(base) + sp.off_c);
+    kda::FwdParams ps = p;
+    ps.Hq = summary_q_heads(pr);
+    ps.seg_len = seg_len;
+    ps.nseg_total = sp.nseg;
+    ps.nseg_used = sp.nseg - 1;
+    ps.s0 = nullptr;
+    ps.sfin = b_seg;
+    ps.flags = kda::kFlagNoOutput;
+    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
+        return cuda_fail(e, "pre_scan (summary) launch");
+    ps.sfin = m_seg;
+    ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0;
+    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
+        return cuda_fail(e, "pre_scan (transition) launch");
+    if ((e = kda::launch_merge(m_seg, b_seg, p.s0, carries, pr.N, sp.nseg, pr.H, sm_count, stream)) !=
+        cudaSuccess)
+        return cuda_fail(e, "merge launch");
+    kda::FwdParams pk = p;
+    pk.seg_len = seg_len;
+    pk.nseg_total = sp.nseg;
+    pk.nseg_used = sp.nseg;
+    pk.s0 = carries;
+    pk.flags = kda::kFlagFinalLastSeg;
+    if ((e = kda::launch_serial(pk, maps, stream)) != cudaSuccess)
+        return cuda_fail(e, "segment-K2 launch");
+    return KDA_OK;
+}
+
 kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                const float* g, const uint16_t* beta, float scale, const float* s0,
                const int32_t* cu, uint16_t* out, float* sfin, cudaStream_t stream,
@@ -468,35 +546,11 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
     if (st != KDA_OK) return st;
     if (pr.T_total == 0 && !sfin) return KDA_OK;
 
-    kda::FwdParams p{};
-    p.q = reinterpret_cast<const __nv_bfloat16*>(q);
-    p.k = reinterpret_cast<const __nv_bfloat16*>(k);
-    p.v = reinterpret_cast<const __nv_bfloat16*>(v);
-    p.g = g;
-    p.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
-    p.s0 = s0;
-    p.sfin = sfin;
-    p.out = reinterpret_cast<__nv_bfloat16*>(out);
-    p.cu = cu;
-    p.T_total = pr.T_total;
-    p.dense_len = pr.dense_len;
-    p.N = pr.N;
-    p.H = pr.H;
-    p.Hq = pr.Hq;
-    p.scale = scale;
-    p.wait_limit = wait_limit;
-    p.debug_flags = debug_flags;
-    p.status = di->status;
+    kda::FwdParams p;
     kda::TensorMaps maps;
-    memset(&maps, 0, sizeof(maps));
-    if (pr.T_total > 0) {
-        if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hq, "q")) ||
-            (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hk, "k")) ||
-            (st = encode_chunk_map(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "v")) ||
-            (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")) ||
-            (st = encode_chunk_map(&maps.out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Ho, "out")))
-            return st;
-    }
+    if ((st = prepare_call(pr, q, k, v, g, beta, scale, s0, cu, out, sfin, wait_limit, debug_flags,
+                           di->status, &p, &maps)) != KDA_OK)
+        return st;
     if (mode == KDA_MODE_AUTO) choose_plan(pr, di->resident_clusters, &mode, &seg_len);
     if (mode == KDA_MODE_SEGMENT && pr.varlen) {
         const VarSegPlan vp = plan_segments_varlen(pr, seg_len);
@@ -550,39 +604,9 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
         if (e != cudaSuccess) return cuda_fail(e, "serial prefill launch");
         return KDA_OK;
     }
-    // Segment-parallel: pre_scan (segment summaries from zero and transitions from the
-    // identity, all segments but the last, in parallel) -> merge (carries) -> segment-K2.
     void* ws = nullptr;
     if ((st = get_workspace(dev, stream, kWsSegment, sp.bytes, &ws)) != KDA_OK) return st;
-    float* b_seg = reinterpret_cast<float*>(static_cast<char*>(ws) + sp.off_b);
-    float* m_seg = reinterpret_cast<float*>(static_cast<char*>(ws) + sp.off_m);
-    float* carries = reinterpret_cast<float*>(static_cast<char*>(ws) + sp.off_c);
-    kda::FwdParams ps = p;
-    ps.Hq = summary_q_heads(pr);
-    ps.seg_len = seg_len;
-    ps.nseg_total = sp.nseg;
-    ps.nseg_used = sp.nseg - 1;
-    ps.s0 = nullptr;
-    ps.sfin = b_seg;
-    ps.flags = kda::kFlagNoOutput;
-    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
-        return cuda_fail(e, "pre_scan (summary) launch");
-    ps.sfin = m_seg;
-    ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0;
-    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
-        return cuda_fail(e, "pre_scan (transition) launch");
-    if ((e = kda::launch_merge(m_seg, b_seg, s0, carries, pr.N, sp.nseg, pr.H, di->sm_count, stream)) !=
-        cudaSuccess)
-        return cuda_fail(e, "merge launch");
-    kda::FwdParams pk = p;
-    pk.seg_len = seg_len;
-    pk.nseg_total = sp.nseg;
-    pk.nseg_used = sp.nseg;
-    pk.s0 = carries;
-    pk.flags = kda::kFlagFinalLastSeg;
-    if ((e = kda::launch_serial(pk, maps, stream)) != cudaSuccess)
-        return cuda_fail(e, "segment-K2 launch");
-    return KDA_OK;
+    return run_dense_segments(pr, p, maps, sp, seg_len, ws, di->sm_count, stream);
 }
 
 }  // namespace
@@ -1038,13 +1062,13 @@ const char* kda_version(void) { return "0.1.0"; }
 // ---------------------------------------------------------------------------
 // Segment-parallel prefill that allocates nothing on the device.
 //
-// Some callers cannot call cudaMalloc at all: code running inside a CUDA graph that is
-// being captured (allocation is not a stream operation), allocators that own every
-// byte of device memory and forbid side allocations, and real-time services that must
-// not risk an allocation failure or the implicit device synchronisation of a first
-// allocation in the middle of a request.  kda_prefill_segment_noalloc() serves them:
-// its scratch (segment summaries, transitions and carries) lives in one fixed
-// file-scope device array, so no call allocates or frees anything.
+// Some callers cannot call cudaMalloc at all: applications whose caching allocator owns
+// every byte of device memory and forbids side allocations, real-time services that must
+// not risk an allocation failure or the device synchronisation a cudaMalloc can imply in
+// the middle of a request, and plugin hosts that give a library no allocation rights.
+// kda_prefill_segment_noalloc() serves them: its scratch (segment summaries, transitions
+// and carries) lives in one fixed file-scope device array, so no call allocates or frees
+// anything.
 namespace {
 
 // 32 MiB: room for 512 fp32 128x128 state slots; a call needs B * H * (3 * nseg - 2).
@@ -1114,68 +1138,16 @@ extern "C" kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const 
     if ((st = noalloc_scratch(dev, &scratch)) != KDA_OK) return st;
     if (pr.T_total == 0 && !final_state) return KDA_OK;
 
-    kda::FwdParams p{};
-    p.q = reinterpret_cast<const __nv_bfloat16*>(q);
-    p.k = reinterpret_cast<const __nv_bfloat16*>(k);
-    p.v = reinterpret_cast<const __nv_bfloat16*>(v);
-    p.g = g;
-    p.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
-    p.s0 = initial_state;
-    p.sfin = final_state;
-    p.out = reinterpret_cast<__nv_bfloat16*>(out);
-    p.cu = nullptr;
-    p.T_total = pr.T_total;
-    p.dense_len = pr.dense_len;
-    p.N = pr.N;
-    p.H = pr.H;
-    p.Hq = pr.Hq;
-    p.scale = scale;
-    p.wait_limit = kDefaultWaitLimit;
-    p.status = di->status;
+    kda::FwdParams p;
     kda::TensorMaps maps;
-    memset(&maps, 0, sizeof(maps));
-    if (pr.T_total > 0) {
-        if ((st = encode_chunk_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hq, "q")) ||
-            (st = encode_chunk_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Hk, "k")) ||
-            (st = encode_chunk_map(&maps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.H, "v")) ||
-            (st = encode_chunk_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.T_total, pr.H, "g")) ||
-            (st = encode_chunk_map(&maps.out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pr.T_total, pr.Ho, "out")))
-            return st;
-    }
+    if ((st = prepare_call(pr, q, k, v, g, beta, scale, initial_state, nullptr, out, final_state,
+                           kDefaultWaitLimit, 0, di->status, &p, &maps)) != KDA_OK)
+        return st;
     if (sp.nseg <= 1) {  // one segment: the plain serial pass, no scratch
         if ((e = kda::launch_serial(p, maps, stream)) != cudaSuccess)
             return cuda_fail(e, "prefill launch");
         return KDA_OK;
     }
-    // Every scratch byte a call reads is written earlier in the same call (summaries and
-    // transitions by pre_scan, carries by merge), so nothing needs clearing first.
-    float* b_seg = reinterpret_cast<float*>(static_cast<char*>(scratch) + sp.off_b);
-    float* m_seg = reinterpret_cast<float*>(static_cast<char*>(scratch) + sp.off_m);
-    float* carries = reinterpret_cast<float*>(static_cast<char*>(scratch) + sp.off_c);
-    kda::FwdParams ps = p;
-    ps.Hq = summary_q_heads(pr);
-    ps.seg_len = segment_len;
-    ps.nseg_total = sp.nseg;
-    ps.nseg_used = sp.nseg - 1;
-    ps.s0 = nullptr;
-    ps.sfin = b_seg;
-    ps.flags = kda::kFlagNoOutput;
-    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
-        return cuda_fail(e, "pre_scan (summary) launch");
-    ps.sfin = m_seg;
-    ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0;
-    if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
-        return cuda_fail(e, "pre_scan (transition) launch");
-    if ((e = kda::launch_merge(m_seg, b_seg, initial_state, carries, pr.N, sp.nseg, pr.H,
-                               di->sm_count, stream)) != cudaSuccess)
-        return cuda_fail(e, "merge launch");
-    kda::FwdParams pk = p;
-    pk.seg_len = segment_len;
-    pk.nseg_total = sp.nseg;
-    pk.nseg_used = sp.nseg;
-    pk.s0 = carries;
-    pk.flags = kda::kFlagFinalLastSeg;
-    if ((e = kda::launch_serial(pk, maps, stream)) != cudaSuccess)
-        return cuda_fail(e, "segment-K2 launch");
-    return KDA_OK;
+    // The same pipeline as segment mode, on the fixed array instead of a workspace.
+    return run_dense_segments(pr, p, maps, sp, segment_len, scratch, di->sm_count, stream);
 }

@@ -61,11 +61,15 @@ extern "C" {
 typedef enum kda_status {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARGUMENT = 1,     /* bad shape, null/misaligned pointer, bad option */
-    KDA_ERR_ALIASING = 2,             /* out overlaps an input; partial state overlap */
+    KDA_ERR_ALIASING = 2,             /* out overlaps an input; partial state overlap (exact
+                                         alias allowed: flashinfer PR #4351, review of
+                                         CheckNoPartialOverlapOrExactAlias) */
     KDA_ERR_UNSUPPORTED_DEVICE = 3,   /* current device is not compute capability 10.3 */
     KDA_ERR_OUT_OF_MEMORY = 4,        /* a workspace allocation failed */
     KDA_ERR_CUDA = 5,                 /* a CUDA runtime call or launch failed */
-    KDA_ERR_CAPTURE_NEEDS_WARMUP = 6, /* a workspace would be allocated during stream capture */
+    KDA_ERR_CAPTURE_NEEDS_WARMUP = 6, /* a workspace would be allocated during stream capture
+                                         (flashinfer PR #4313, review of EncodeTmaPointers:
+                                         warm the workspace before capture) */
     KDA_ERR_DEVICE_TIMEOUT = 7        /* a device-side bounded wait ran out (status word) */
 } kda_status;
 
@@ -166,11 +170,13 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
                             void* stream, const kda_options* opts);
 
 /* kda_prefill_segment_noalloc -- segment-parallel prefill that allocates no device
- * memory.  The pages have no counterpart: this entry point exists for callers that
- * cannot call cudaMalloc (code inside a stream capture, applications whose allocator
- * owns all device memory, services that must not allocate in a request), as a variant
- * of segment mode (kda_prefill_ex with KDA_MODE_SEGMENT) whose scratch lives in one
- * fixed 32 MiB device array inside the library.
+ * memory.  The pages have no counterpart.  Some callers of a prefill cannot call
+ * cudaMalloc: applications whose caching allocator owns all of device memory and
+ * forbids side allocations, real-time services that must not risk an allocation failure
+ * or the device synchronisation a cudaMalloc can imply in the middle of a request, and
+ * plugin hosts that give a library no allocation rights.  This entry point is segment
+ * mode (kda_prefill_ex with KDA_MODE_SEGMENT, the same kernels on the same plan) with its
+ * scratch in one fixed 32 MiB device array inside the library instead of a workspace.
  *   Arguments as kda_prefill for dense input (no cu_seqlens); segment_len is the
  *   segment length in tokens, a positive multiple of 16.
  *   Limit: B * H * (3 * nseg - 2) <= 512, nseg = ceil(seq_len / segment_len) (each
@@ -178,8 +184,8 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
  *   device work.  A single segment needs no scratch.
  *   The array is shared by every call in the process and keeps the last call's
  *   contents; no part of it needs to start at zero (each call writes every byte it
- *   reads).  Calls that overlap on the GPU (other streams, other threads) race on it:
- *   serialise them.
+ *   reads before reading it).  Calls that overlap on the GPU (other streams, other
+ *   threads) race on it: serialise them.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call before any
  *   stream capture.  Every GPU that loads the library holds the 32 MiB until exit. */
@@ -202,7 +208,7 @@ kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q
  * a state that stays resident on the device.  The pages mention a decode registration
  * beside the prefill (flashinfer PR #4313 "feat(cake_kda): share recurrent prefill
  * kernels across SM100 family", publication notes) and a bf16 final state in the
- * reference facade (flashinfer PR #4351 review of kda_prefill.py); neither gives the
+ * reference facade (flashinfer PR #4313, review of kda_prefill.py); neither gives the
  * kernel, so this one is the recurrence itself, HBM-bound on the state.
  *   shape          dense only: batch = N sequences, seq_len = T tokens of each
  *                  (T >= 0; the cost grows linearly in T, use kda_prefill for long
@@ -228,8 +234,11 @@ kda_status kda_decode(const kda_shape* shape, const uint16_t* q, const uint16_t*
                       uint16_t* out, void* stream);
 
 /* Bytes of device workspace a call with this shape and these options uses
- * (0 for serial mode).  A shape with num_seqs > 0 is taken as packed varlen input
- * (segment mode then sizes for at most num_seqs + seq_len / segment_len segments).
+ * (0 for serial mode).  The segment pipeline's scratch (per-segment summaries,
+ * transitions and carries: cuLA PR #103, review of the CP driver's _get_scratch, which
+ * sizes b_seg, m_seg, carries and seg_final per shape) is reported here so a caller can
+ * budget it before the first call.  A shape with num_seqs > 0 is taken as packed varlen
+ * input (segment mode then sizes for at most num_seqs + seq_len / segment_len segments).
  * kda_prefill_host holds, besides, an arena the size of its tensors.  No device work,
  * except that KDA_MODE_AUTO reads the current device's resident cluster count to
  * resolve the plan; *bytes is written on success. */
@@ -253,17 +262,34 @@ kda_status kda_plan(const kda_shape* shape, int32_t varlen, int32_t resident_clu
 
 /* Reads and clears the device status word of the current device after
  * synchronising `stream`.  *code receives KDA_OK, KDA_ERR_INVALID_ARGUMENT
- * (malformed cu_seqlens contents seen by a kernel) or KDA_ERR_DEVICE_TIMEOUT. */
+ * (malformed cu_seqlens contents seen by a kernel) or KDA_ERR_DEVICE_TIMEOUT.
+ * The pages validate on the host and abort the call with a message (flashinfer PR
+ * #4313, review of flashkda_binding_common.cuh: the TVM_FFI_ICHECK target, shape and
+ * capacity checks) and record a device-side hazard only in review (flashinfer PR #4351,
+ * review of the beta packing: a kernel that reads uninitialised workspace); conditions
+ * that only a kernel can see (cu_seqlens contents, a bounded wait that ran out) are
+ * therefore kept in a per-device word the kernels write and this call reads. */
 kda_status kda_get_device_status(void* stream, int32_t* code);
 
 /* Frees every workspace the library holds on `device` (-1 = all devices).
- * The caller must ensure no call using them is still running. */
+ * The caller must ensure no call using them is still running.  Workspaces are keyed by
+ * (device, stream, kind), at most 8 of them, least recently used evicted first: the
+ * pages' scratch cache raced across streams because its key lacked the stream (cuLA PR
+ * #103, review of _get_scratch) and their per-stream workspace maps grew without bound
+ * (flashinfer PR #4313, review of kda_prefill.py, which asks for a bound or an eviction
+ * path); this call is the explicit release. */
 kda_status kda_release_workspaces(int32_t device);
 
-/* Static description of a status code. */
+/* Static description of a status code.  The pages' bindings fail with a message per
+ * check (flashinfer PR #4313, review of flashkda_binding_common.cuh; flashinfer PR #4351,
+ * review of CheckNoPartialOverlapOrExactAlias for KDA_ERR_ALIASING; the capture guard
+ * of EncodeTmaPointers, "prepare_descriptors must be 0 during CUDA graph capture", for
+ * KDA_ERR_CAPTURE_NEEDS_WARMUP); across a C ABI that becomes a code plus this text. */
 const char* kda_status_string(kda_status status);
 
-/* Message of the last failing call on this host thread ("" if none). */
+/* Message of the last failing call on this host thread ("" if none): the specific
+ * reason (which argument, which size), as the pages' per-check messages give it
+ * (flashinfer PR #4313, review of flashkda_binding_common.cuh). */
 const char* kda_last_error_message(void);
 
 /* Library version, e.g. "0.1.0". */
