@@ -10,7 +10,8 @@
 namespace kda {
 
 constexpr int kD = 128;     // Dk = Dv
-constexpr int kChunk = 16;  // rows per chunk
+constexpr int kChunk = 16;  // rows per chunk (the WY solve's diagonal blocks)
+constexpr int kStep = 32;   // tokens the state chain advances per step (two chunks)
 
 // Device status codes (same values as kda_status).
 constexpr int32_t kStatusOk = 0;
@@ -49,6 +50,8 @@ struct FwdParams {
     int32_t flags;        // kFlag* below
     const int32_t* seg_start;  // varlen segment table [N + 1] (device), or nullptr
     int32_t rows;         // varlen segment launches: rows launched (an upper bound)
+    int32_t s0_bf16;      // 1: s0 holds bf16 values (same layout), else fp32
+    int32_t sfin_bf16;    // 1: sfin is written as bf16 (round to nearest even), else fp32
 };
 
 // The recurrent decode step: T tokens of each of N dense sequences, H heads.
@@ -151,7 +154,7 @@ __device__ __forceinline__ bool seq_range(const FwdParams& p, int n, int64_t& bo
     return true;
 }
 
-// TMA descriptors of the [T_total][H][128] inputs, box {128, 1, 16} (one chunk of
+// TMA descriptors of the [T_total][H][128] inputs, box {128, 1, 32} (one chain step of
 // one head).  Encoded on the host, passed to kernels as __grid_constant__ params.
 struct TensorMaps {
     CUtensorMap q, k, v, g;
