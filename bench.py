@@ -42,7 +42,7 @@ STATE_BYTES = 128 * 128 * 4
 # Tensor-core operands are bf16 (fp32 accumulation); the state, decays and the WY
 # solve are fp32.
 COMPUTE_DTYPE = "bf16"
-_FWD_SOURCES = ["chunked_kda_delta_gb300/csrc/kda_fwd.cu",
+_FWD_SOURCES = ["chunked_kda_delta_gb300/csrc/kda_fwd_tc.cu",
                 "chunked_kda_delta_gb300/csrc/kda_ptx.cuh",
                 "chunked_kda_delta_gb300/csrc/kda_internal.cuh"]
 _DECODE_SOURCES = ["chunked_kda_delta_gb300/csrc/kda_decode.cu",
@@ -51,8 +51,8 @@ KERNEL_SOURCES = {"serial": _FWD_SOURCES,
                   "segment": _FWD_SOURCES + ["chunked_kda_delta_gb300/csrc/kda_merge.cu"],
                   "auto": _FWD_SOURCES + ["chunked_kda_delta_gb300/csrc/kda_merge.cu"],
                   "decode_fp32": _DECODE_SOURCES, "decode_bf16": _DECODE_SOURCES}
-KERNEL_NAMES = {"serial": "kda_fwd_kernel",
-                "segment": "kda_fwd_kernel x3 + kda_merge_kernel (whole step)",
+KERNEL_NAMES = {"serial": "kda_fwd_tc_kernel",
+                "segment": "kda_fwd_tc_kernel x3 + kda_merge_kernel (whole step)",
                 "auto": "the plan the library picks (whole step)",
                 "decode_fp32": "kda_decode_kernel<float>",
                 "decode_bf16": "kda_decode_kernel<bf16>"}

@@ -198,7 +198,7 @@ kda_status encode_chunk_map(CUtensorMap* m, const void* base, CUtensorMapDataTyp
     if (st != KDA_OK) return st;
     cuuint64_t dims[3] = {(cuuint64_t)kda::kD, (cuuint64_t)H, (cuuint64_t)T};
     cuuint64_t strides[2] = {(cuuint64_t)kda::kD * elem, (cuuint64_t)H * kda::kD * elem};
-    cuuint32_t box[3] = {(cuuint32_t)kda::kD, 1, (cuuint32_t)kda::kStep};
+    cuuint32_t box[3] = {(cuuint32_t)kda::kD, 1, (cuuint32_t)kda::kChunk};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

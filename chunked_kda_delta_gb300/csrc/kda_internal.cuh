@@ -10,8 +10,7 @@
 namespace kda {
 
 constexpr int kD = 128;     // Dk = Dv
-constexpr int kChunk = 16;  // rows per chunk (the WY solve's diagonal blocks)
-constexpr int kStep = 32;   // tokens the state chain advances per step (two chunks)
+constexpr int kChunk = 16;  // rows per chunk
 
 // Device status codes (same values as kda_status).
 constexpr int32_t kStatusOk = 0;
@@ -154,7 +153,7 @@ __device__ __forceinline__ bool seq_range(const FwdParams& p, int n, int64_t& bo
     return true;
 }
 
-// TMA descriptors of the [T_total][H][128] inputs, box {128, 1, 32} (one chain step of
+// TMA descriptors of the [T_total][H][128] inputs, box {128, 1, 16} (one chunk of
 // one head).  Encoded on the host, passed to kernels as __grid_constant__ params.
 struct TensorMaps {
     CUtensorMap q, k, v, g;
