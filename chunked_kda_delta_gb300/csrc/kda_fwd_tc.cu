@@ -16,9 +16,13 @@
 //   O      = scale (Qtil S + Mq delta),  Qtil = Q o exp(gam)
 //   S     <- Diag(exp gam_C) S + Kbar^T delta,  Kbar_r = k_r o exp(gam_C - gam_r)
 // exp(gam_r - gam_s) is factored through the chunk's row 7 as
-// exp(gam_r - gam_ref) exp(gam_ref - gam_s); each factor stays in fp32 range while
-// the log-decay accumulated over 8 consecutive tokens of a channel is above ~-80.
-// K o exp(gam) and Q o exp(gam) are formed as (K o exp(gam - gam_ref)) exp(gam_ref).
+// exp(gam_r - gam_ref) exp(gam_ref - gam_s), and K o exp(gam), Q o exp(gam) are formed as
+// (K o exp(gam - gam_ref)) exp(gam_ref).  Each factor is at most e^kFastLimit while a
+// channel's cumulative log-decay falls by at most kFastLimit over the chunk.  A chunk with
+// channels beyond that (strong decay) takes strong_decay_chunk() as well: those channels
+// leave the factored Grams, their terms k_r k_s exp(gam_r - gam_s) (q_r for Mq) are
+// formed pair by pair with the exponent taken directly, and their K o exp(gam),
+// Q o exp(gam) and Kbar are formed directly, so no factor exceeds 1 for g <= 0.
 //
 // Mapping (transposed so the 128-wide value dim is the MMA's M):
 //   TMEM holds S^T (lane j = value column, column i = key row) in fp32.
@@ -62,6 +66,7 @@ using namespace ptx;
 constexpr int kK1Groups = 3;                    // K1 groups, chunk c -> group c % 3
 constexpr int kThreads = 32 * (1 + 4 * kK1Groups);  // 416
 constexpr int kRef = 7;
+constexpr float kFastLimit = 80.f;  // largest log-decay fall over a chunk for the factored path
 constexpr uint32_t kTmemCols = 512;
 // Bound of the waits that drain in-flight copies and MMAs before exit; independent of
 // the caller's wait limit so that an early exit never leaves asynchronous work behind.
@@ -98,8 +103,11 @@ constexpr uint32_t kLbo = 128, kSboB1 = 2048, kSboB2 = 256, kSboB3 = 256;
 // K1 group scratch: padded bf16 staging rows (136 elements), exp(gam_ref), A, Tb, beta.
 constexpr int kStRow = 272, kStArr = 16 * kStRow;
 enum { ST_KQ = 0, ST_QQ, ST_KK, ST_VV, ST_NUM };
+// Strong-decay chunks also use: a flag word and the 128-bit channel mask, and the exact
+// Gram terms (A^T, then Mq^T, fp32 [16][16] each).
 constexpr int kGEref = ST_NUM * kStArr, kGA = kGEref + 512, kGTb = kGA + 1024,
-              kGBeta = kGTb + 768, kGrpBytes = kGBeta + 64;
+              kGBeta = kGTb + 768, kGSlow = kGBeta + 64, kGCorr = kGSlow + 32,
+              kGrpBytes = kGCorr + 2048;
 // Shared memory map.  K1 CTA: input ring, 2 group scratches, 2 local operand stages.
 // K2 CTA: receive ring at offset 0.  Barriers sit at the same offset in both.
 constexpr int kSmIn = 0;
@@ -164,6 +172,97 @@ __device__ __forceinline__ uint32_t b3_off(int n, int k) {
 
 __device__ __forceinline__ void record(int32_t* status, int32_t code) {
     atomicCAS(status, kStatusOk, code);
+}
+
+// A chunk with strong-decay channels (a channel whose cumulative log-decay falls by more
+// than kFastLimit over the chunk), run by the 128 threads of its K1 group after phase 1
+// and before phase 2; `t` = thread in the group, (pc, hr) its channel pair and row half
+// as in phase 1.  Phase 1 has already written the factored operands of every channel;
+// this pass
+//   - turns g in the input stage into the cumulative log-decay gam (rows past C add 0),
+//   - for each strong-decay channel c: stages K o exp(gam) and Q o exp(gam) (eref 1),
+//     zero in the Gram's right operand (so the factored Grams leave c out), and writes
+//     Kbar = K o exp(gam_C - gam) into B2; and records c in the channel mask,
+//   - writes the exact Gram terms of the masked channels into corr:
+//       corr[s * 16 + r]       = beta_r sum_c k_r[c] k_s[c] exp(gam_r[c] - gam_s[c]), s < r
+//       corr[256 + s * 16 + r] = sum_c q_r[c] k_s[c] exp(gam_r[c] - gam_s[c]),      s <= r
+//     (every other entry 0), which phase 2 adds to the factored Grams.
+// No factor formed here exceeds 1 for g <= 0.  Ends with the group's barrier passed.
+__device__ __noinline__ void strong_decay_chunk(unsigned char* in, unsigned char* grp, unsigned char* ob, int C,
+                                                int t, uint32_t nbar) {
+    const int pc = t & 63, hr = t >> 6;
+    unsigned char* st = grp;
+    float* eref = reinterpret_cast<float*>(grp + kGEref);
+    unsigned char* b2 = ob + kB2;
+    uint32_t* mask = reinterpret_cast<uint32_t*>(grp + kGSlow) + 4;
+    float* corr = reinterpret_cast<float*>(grp + kGCorr);
+    const float* beta = reinterpret_cast<const float*>(grp + kGBeta);
+    float* gam = reinterpret_cast<float*>(in + kInG);
+    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(in + kInQ);
+    const __nv_bfloat16* k = reinterpret_cast<const __nv_bfloat16*>(in + kInK);
+    if (t < 4) mask[t] = 0u;
+    reinterpret_cast<float4*>(corr)[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    named_bar_sync(nbar, 128);  // every thread has read g in phase 1
+    if (hr == 0) {
+        float2 a = make_float2(0.f, 0.f);
+        float2* g2 = reinterpret_cast<float2*>(gam);
+        for (int r = 0; r < kChunk; ++r) {
+            a = add2(a, r < C ? g2[r * 64 + pc] : make_float2(0.f, 0.f));
+            g2[r * 64 + pc] = a;
+        }
+    }
+    named_bar_sync(nbar, 128);
+    for (int e = 0; e < 2; ++e) {
+        const int c = 2 * pc + e;
+        const float gc = gam[(kChunk - 1) * kD + c];
+        if (gam[c] - gc <= kFastLimit) continue;
+        if (hr == 0) {
+            atomicOr(mask + (c >> 5), 1u << (c & 31));
+            eref[c] = 1.f;
+        }
+        for (int rr = 0; rr < 8; ++rr) {
+            const int r = 8 * hr + rr;
+            const bool valid = r < C;
+            const float kr = valid ? __bfloat162float(k[r * kD + c]) : 0.f;
+            const float qr = valid ? __bfloat162float(q[r * kD + c]) : 0.f;
+            const float gr = gam[r * kD + c];
+            const float eg = ex2(gr * kLog2e), egc = ex2((gc - gr) * kLog2e);
+            __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(st + r * kStRow) + c;
+            row[ST_KQ * kStArr / 2] = __float2bfloat16_rn(kr * eg);
+            row[ST_QQ * kStArr / 2] = __float2bfloat16_rn(qr * eg);
+            row[ST_KK * kStArr / 2] = __float2bfloat16_rn(0.f);
+            *reinterpret_cast<__nv_bfloat16*>(b2 + (c >> 3) * kSboB2 + hr * kLbo + (c & 7) * 16 + rr * 2) =
+                __float2bfloat16_rn(kr * egc);
+        }
+    }
+    named_bar_sync(nbar, 128);
+    // Exact terms: pairs 0 .. 119 of A (s < r), 120 .. 255 of Mq (s <= r), rows in order.
+    for (int idx = t; idx < 256; idx += 128) {
+        const bool is_q = idx >= 120;
+        const int pi = is_q ? idx - 120 : idx;
+        int r = is_q ? 0 : 1, base = 0;
+        while (base + (is_q ? r + 1 : r) <= pi) {
+            base += is_q ? r + 1 : r;
+            ++r;
+        }
+        const int sc = pi - base;
+        if (r >= C || sc >= C) continue;
+        const __nv_bfloat16* a = is_q ? q : k;
+        float acc = 0.f;
+        for (int w = 0; w < 4; ++w) {
+            uint32_t m = mask[w];
+            while (m != 0u) {
+                const int c = 32 * w + __ffs(m) - 1;
+                m &= m - 1u;
+                const float f = ex2((gam[r * kD + c] - gam[sc * kD + c]) * kLog2e);
+                acc = fmaf(__bfloat162float(a[r * kD + c]) * __bfloat162float(k[sc * kD + c]), f, acc);
+            }
+        }
+        if (is_q) corr[256 + sc * 16 + r] = acc;
+        else corr[sc * 16 + r] = beta[r] * acc;
+    }
+    fence_proxy_async_smem();  // B2 is shipped by a bulk copy
+    named_bar_sync(nbar, 128);
 }
 
 // C[r][s] = sum_c A[r][c] B[s][c] for 16x16 tiles over 128 channels; A and B are
@@ -330,12 +429,18 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float* Asm = reinterpret_cast<float*>(grp + kGA);
         __nv_bfloat16* Tb = reinterpret_cast<__nv_bfloat16*>(grp + kGTb);
         float* bet = reinterpret_cast<float*>(grp + kGBeta);
+        // Strong-decay chunks: flag word (set by any thread of the group in phase 1, read
+        // after the group's barrier), channel mask and exact Gram terms.
+        volatile uint32_t* slow_flag = reinterpret_cast<volatile uint32_t*>(grp + kGSlow);
+        float* corr = reinterpret_cast<float*>(grp + kGCorr);
         unsigned char* ob = smem + kSmOutLocal + gi * kOutBytes;
         const float2 l2e2 = make_float2(kLog2e, kLog2e), nl2e2 = make_float2(-kLog2e, -kLog2e);
         const bool zero_v = (p.flags & kFlagZeroV) != 0;
         const bool with_out = (p.flags & kFlagNoOutput) == 0;
         for (int c = gi; c < nchunks; c += kK1Groups) {
             const int s = c % kInStages;
+            // (every thread of the group is past the previous chunk's phase 2)
+            if (kt == 0) *slow_flag = 0u;
             // One thread waits for the input tiles; the group barrier publishes them.
             bool ok = !fail_flag[gi];
             if (kt == kt_wait) ok = ok && mbar_wait(bar(BAR_IN_FULL + s), (c / kInStages) & 1, lim);
@@ -366,6 +471,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float2 lastl = mul2f(gl[kChunk - 1], l2e2);
             const float2 ecr = ex2x2(add2(lastl, nrefl));     // exp(gam_C - gam_ref)
             const float2 gcl = ex2x2(lastl);  // exp(gam_C), written to the operand buffer below
+            // (gam is non-increasing for g <= 0: its fall over the chunk is gam_0 - gam_15)
+            if (gl[0].x - gl[kChunk - 1].x > kFastLimit || gl[0].y - gl[kChunk - 1].y > kFastLimit)
+                *slow_flag = 1u;
             if (hr == 0) reinterpret_cast<float2*>(eref_sm)[pc] = ex2x2(refl);
             const uint32_t* q2 = reinterpret_cast<const uint32_t*>(in + kInQ);
             const uint32_t* k2 = reinterpret_cast<const uint32_t*>(in + kInK);
@@ -409,7 +517,9 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (kt == kt_wait) record(p.status, kStatusTimeout);
                 break;
             }
-            if (kt == kt_wait) mbar_arrive(bar(BAR_IN_EMPTY + s));  // input tiles consumed
+            // (the flag was set before the barrier above: the same answer in every thread)
+            const bool strong = *slow_flag != 0u;
+            if (kt == kt_wait && !strong) mbar_arrive(bar(BAR_IN_EMPTY + s));  // input tiles consumed
             {   // Kbar rows 2pc, 2pc+1 of B2 (N = key channel, K = chunk row), exp(gam_C)
                 unsigned char* b2 = ob + kB2;
                 const int c0 = 2 * pc, c1 = 2 * pc + 1;
@@ -418,6 +528,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 *reinterpret_cast<uint4*>(b2 + (c1 >> 3) * kSboB2 + hr * kLbo + (c1 & 7) * 16) =
                     make_uint4(kb1[0], kb1[1], kb1[2], kb1[3]);
                 if (hr == 0) reinterpret_cast<float2*>(ob + kGC)[pc] = gcl;
+            }
+            if (strong) {
+                strong_decay_chunk(smem + kSmIn + s * kInBytes, grp, ob, C, kt, nbar);
+                if (kt == kt_wait) mbar_arrive(bar(BAR_IN_EMPTY + s));  // input tiles consumed
             }
 
             // Phase 2 (by role kr): 0 Gram A and the WY solve; 1 Gram Mq; 2-3 write
@@ -436,6 +550,10 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             Asm[sc * 16 + r] = sc < r ? bet[r] * acc[nt][e] : 0.f;  // A^T
                         }
                     __syncwarp();
+                    if (*slow_flag != 0u) {
+                        for (int i = lane; i < 256; i += 32) Asm[i] += corr[i];
+                        __syncwarp();
+                    }
                     if (lane < 16) {
                         // Column sc of T = (I + A)^{-1} by right-looking forward substitution:
                         // once x_m is final, x_r -= A[r][m] x_m for every r > m.  The updates
@@ -463,6 +581,13 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     }
                 } else {
                     unsigned char* b3 = ob + kB3;
+                    if (*slow_flag != 0u) {
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                acc[nt][e] += corr[256 + (8 * nt + 2 * t + (e & 1)) * 16 + g + 8 * (e >> 1)];
+                    }
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
