@@ -285,12 +285,17 @@ kda_status validate_shape(const kda_shape* s, bool varlen, Problem* pr) {
 }
 
 kda_status validate_options(const kda_options* o, const Problem& pr, int32_t* mode,
-                            int32_t* seg_len, int64_t* wait_limit, int32_t* debug_flags) {
+                            int32_t* seg_len, int64_t* wait_limit, int32_t* debug_flags,
+                            int32_t* state_bf16 = nullptr) {
     *mode = KDA_MODE_SERIAL;
     *seg_len = 8192;
     *wait_limit = kDefaultWaitLimit;
     *debug_flags = 0;
+    if (state_bf16) *state_bf16 = 0;
     if (!o) return KDA_OK;
+    if (o->state_dtype != KDA_STATE_F32 && o->state_dtype != KDA_STATE_BF16)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "unknown state_dtype %d", o->state_dtype);
+    if (state_bf16) *state_bf16 = o->state_dtype == KDA_STATE_BF16;
     if (o->debug_flags & ~KDA_DEBUG_STALL_WAIT)
         return fail(KDA_ERR_INVALID_ARGUMENT, "unknown debug_flags bits 0x%x", o->debug_flags);
     if (o->host_pieces < 0 || o->host_pieces > kMaxHostPieces)
@@ -458,9 +463,10 @@ SegPlan plan_segments(const Problem& pr, int32_t seg_len) {
 
 // Kernel parameters of one call (pointers, sizes, wait limit, status word) and the TMA
 // descriptors of its tensors; shared by every entry point that launches the prefill.
+// s0 / sfin hold fp32 states, or bf16 ones when s0_bf16 / sfin_bf16.
 kda_status prepare_call(const Problem& pr, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                        const float* g, const uint16_t* beta, float scale, const float* s0,
-                        const int32_t* cu, uint16_t* out, float* sfin, int64_t wait_limit,
+                        const float* g, const uint16_t* beta, float scale, const void* s0, int32_t s0_bf16,
+                        const int32_t* cu, uint16_t* out, void* sfin, int32_t sfin_bf16, int64_t wait_limit,
                         int32_t debug_flags, int32_t* status, kda::FwdParams* p,
                         kda::TensorMaps* maps) {
     *p = kda::FwdParams{};
@@ -470,7 +476,9 @@ kda_status prepare_call(const Problem& pr, const uint16_t* q, const uint16_t* k,
     p->g = g;
     p->beta = reinterpret_cast<const __nv_bfloat16*>(beta);
     p->s0 = s0;
+    p->s0_bf16 = s0 ? s0_bf16 : 0;
     p->sfin = sfin;
+    p->sfin_bf16 = sfin ? sfin_bf16 : 0;
     p->out = reinterpret_cast<__nv_bfloat16*>(out);
     p->cu = cu;
     p->T_total = pr.T_total;
@@ -512,7 +520,9 @@ kda_status run_dense_segments(const Problem& pr, const kda::FwdParams& p, const 
     ps.nseg_total = sp.nseg;
     ps.nseg_used = sp.nseg - 1;
     ps.s0 = nullptr;
-    ps.sfin = b_seg;
+    ps.s0_bf16 = 0;
+    ps.sfin = b_seg;  // summaries and transitions stay fp32
+    ps.sfin_bf16 = 0;
     ps.flags = kda::kFlagNoOutput;
     if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
         return cuda_fail(e, "pre_scan (summary) launch");
@@ -520,14 +530,15 @@ kda_status run_dense_segments(const Problem& pr, const kda::FwdParams& p, const 
     ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0;
     if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
         return cuda_fail(e, "pre_scan (transition) launch");
-    if ((e = kda::launch_merge(m_seg, b_seg, p.s0, carries, pr.N, sp.nseg, pr.H, sm_count, stream)) !=
-        cudaSuccess)
+    if ((e = kda::launch_merge(m_seg, b_seg, p.s0, p.s0_bf16, carries, pr.N, sp.nseg, pr.H, sm_count,
+                               stream)) != cudaSuccess)
         return cuda_fail(e, "merge launch");
     kda::FwdParams pk = p;
     pk.seg_len = seg_len;
     pk.nseg_total = sp.nseg;
     pk.nseg_used = sp.nseg;
-    pk.s0 = carries;
+    pk.s0 = carries;  // fp32; the final state keeps the caller's type
+    pk.s0_bf16 = 0;
     pk.flags = kda::kFlagFinalLastSeg;
     if ((e = kda::launch_serial(pk, maps, stream)) != cudaSuccess)
         return cuda_fail(e, "segment-K2 launch");
@@ -535,8 +546,8 @@ kda_status run_dense_segments(const Problem& pr, const kda::FwdParams& p, const 
 }
 
 kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-               const float* g, const uint16_t* beta, float scale, const float* s0,
-               const int32_t* cu, uint16_t* out, float* sfin, cudaStream_t stream,
+               const float* g, const uint16_t* beta, float scale, const void* s0, int32_t s0_bf16,
+               const int32_t* cu, uint16_t* out, void* sfin, int32_t sfin_bf16, cudaStream_t stream,
                int32_t mode, int32_t seg_len, int64_t wait_limit, int32_t debug_flags) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -548,8 +559,8 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
 
     kda::FwdParams p;
     kda::TensorMaps maps;
-    if ((st = prepare_call(pr, q, k, v, g, beta, scale, s0, cu, out, sfin, wait_limit, debug_flags,
-                           di->status, &p, &maps)) != KDA_OK)
+    if ((st = prepare_call(pr, q, k, v, g, beta, scale, s0, s0_bf16, cu, out, sfin, sfin_bf16, wait_limit,
+                           debug_flags, di->status, &p, &maps)) != KDA_OK)
         return st;
     if (mode == KDA_MODE_AUTO) choose_plan(pr, di->resident_clusters, &mode, &seg_len);
     if (mode == KDA_MODE_SEGMENT && pr.varlen) {
@@ -575,7 +586,9 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
             ps.seg_start = table;
             ps.rows = (int32_t)vp.rows;
             ps.s0 = nullptr;
-            ps.sfin = b_seg;
+            ps.s0_bf16 = 0;
+            ps.sfin = b_seg;  // summaries and transitions stay fp32
+            ps.sfin_bf16 = 0;
             ps.flags = kda::kFlagNoOutput | kda::kFlagSkipLastSeg;
             if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
                 return cuda_fail(e, "pre_scan (summary) launch");
@@ -583,15 +596,15 @@ kda_status run(const Problem& pr, const uint16_t* q, const uint16_t* k, const ui
             ps.flags = kda::kFlagNoOutput | kda::kFlagZeroV | kda::kFlagIdentityS0 | kda::kFlagSkipLastSeg;
             if ((e = kda::launch_serial(ps, maps, stream)) != cudaSuccess)
                 return cuda_fail(e, "pre_scan (transition) launch");
-            if ((e = kda::launch_merge(m_seg, b_seg, s0, carries, pr.N, 0, pr.H, di->sm_count, stream,
-                                      table)) !=
-                cudaSuccess)
+            if ((e = kda::launch_merge(m_seg, b_seg, p.s0, p.s0_bf16, carries, pr.N, 0, pr.H, di->sm_count,
+                                      stream, table)) != cudaSuccess)
                 return cuda_fail(e, "merge launch");
             kda::FwdParams pk = p;
             pk.seg_len = seg_len;
             pk.seg_start = table;
             pk.rows = (int32_t)vp.rows;
-            pk.s0 = carries;
+            pk.s0 = carries;  // fp32; the final state keeps the caller's type
+            pk.s0_bf16 = 0;
             pk.flags = kda::kFlagFinalLastSeg;
             if ((e = kda::launch_serial(pk, maps, stream)) != cudaSuccess)
                 return cuda_fail(e, "segment-K2 launch");
@@ -615,20 +628,20 @@ extern "C" {
 
 kda_status kda_prefill_ex(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
                           const uint16_t* v, const float* g, const uint16_t* beta, float scale,
-                          const float* initial_state, const int32_t* cu_seqlens, uint16_t* out,
-                          float* final_state, void* stream, const kda_options* opts) {
+                          const void* initial_state, const int32_t* cu_seqlens, uint16_t* out,
+                          void* final_state, void* stream, const kda_options* opts) {
     t_last_error[0] = '\0';
     Problem pr{};
     kda_status st = validate_shape(shape, cu_seqlens != nullptr, &pr);
     if (st != KDA_OK) return st;
-    int32_t mode, seg_len, debug_flags;
+    int32_t mode, seg_len, debug_flags, sbf;
     int64_t wait_limit;
-    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit, &debug_flags)) != KDA_OK)
+    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit, &debug_flags, &sbf)) != KDA_OK)
         return st;
     if ((st = validate_pointers(pr, q, k, v, g, beta, scale, initial_state, cu_seqlens, out,
-                                final_state)) != KDA_OK)
+                                final_state, sbf ? 2 : 4)) != KDA_OK)
         return st;
-    return run(pr, q, k, v, g, beta, scale, initial_state, cu_seqlens, out, final_state,
+    return run(pr, q, k, v, g, beta, scale, initial_state, sbf, cu_seqlens, out, final_state, sbf,
                (cudaStream_t)stream, mode, seg_len, wait_limit, debug_flags);
 }
 
@@ -759,17 +772,17 @@ std::vector<HostPiece> host_pieces(const Problem& pr, const int32_t* cu, int wan
 
 kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
                             const uint16_t* v, const float* g, const uint16_t* beta,
-                            float scale, const float* initial_state,
-                            const int32_t* cu_seqlens, uint16_t* out, float* final_state,
+                            float scale, const void* initial_state,
+                            const int32_t* cu_seqlens, uint16_t* out, void* final_state,
                             void* stream_, const kda_options* opts) {
     t_last_error[0] = '\0';
     cudaStream_t stream = (cudaStream_t)stream_;
     Problem pr{};
     kda_status st = validate_shape(shape, cu_seqlens != nullptr, &pr);
     if (st != KDA_OK) return st;
-    int32_t mode, seg_len, debug_flags;
+    int32_t mode, seg_len, debug_flags, sbf;
     int64_t wait_limit;
-    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit, &debug_flags)) != KDA_OK)
+    if ((st = validate_options(opts, pr, &mode, &seg_len, &wait_limit, &debug_flags, &sbf)) != KDA_OK)
         return st;
     if (pr.T_total > 0 && (!q || !k || !v || !g || !beta || !out))
         return fail(KDA_ERR_INVALID_ARGUMENT, "a required host pointer is NULL");
@@ -785,7 +798,8 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     DeviceInfo* di = nullptr;
     if ((st = device_info(dev, &di)) != KDA_OK) return st;
-    const Sizes sz = sizes_of(pr);
+    const size_t se = sbf ? 2 : 4;  // bytes of a state element (the caller's type)
+    const Sizes sz = sizes_of(pr, se);
     // Pieces: serial plans only (segment mode needs the whole sequence in one call).
     int32_t plan_mode = mode, plan_len = 0;  // the whole problem's plan, AUTO resolved
     if (mode == KDA_MODE_AUTO) choose_plan(pr, di->resident_clusters, &plan_mode, &plan_len);
@@ -800,16 +814,18 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
     const int32_t piece_mode = P > 1 ? plan_mode : mode;
 
     // Device arena: the whole problem's tensors at their natural offsets, the offsets of
-    // every piece rebased to its first token, and one state table (final states, or the
-    // state carried between token blocks).
+    // every piece rebased to its first token, the final states (the caller's type) and,
+    // for token blocks, the fp32 state carried from block to block.
     const size_t sb = sz.state;
-    const bool need_fin = final_state != nullptr || blocks;
+    const size_t D = kda::kD, st_elems = (size_t)pr.H * D * D;  // one sequence's states
     const size_t cub = pr.varlen ? (size_t)(pr.N + P) * 4 : 0;
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     const size_t off_q = 0, off_k = off_q + up(sz.q), off_v = off_k + up(sz.k),
-                 off_g = off_v + up(sz.v), off_b = off_g + up(sz.g), off_s0 = off_b + up(sz.beta),
-                 off_cu = off_s0 + (initial_state ? up(sb) : 0), off_out = off_cu + up(cub),
-                 off_fin = off_out + up(sz.out), total = off_fin + (need_fin ? up(sb) : 0);
+                 off_g = off_v + up(sz.v), off_b = off_g + up(sz.g),
+                 off_s0 = off_b + up(sz.beta), off_cu = off_s0 + (initial_state ? up(sb) : 0),
+                 off_out = off_cu + up(cub), off_fin = off_out + up(sz.out),
+                 off_carry = off_fin + (final_state ? up(sb) : 0),
+                 total = off_carry + (blocks ? up(st_elems * 4) : 0);
     void* base = nullptr;
     if ((st = get_workspace(dev, stream, kWsHostArena, total, &base)) != KDA_OK) return st;
     HostPipe* hp = nullptr;
@@ -820,11 +836,13 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
     uint16_t* d_v = reinterpret_cast<uint16_t*>(b + off_v);
     float* d_g = reinterpret_cast<float*>(b + off_g);
     uint16_t* d_beta = reinterpret_cast<uint16_t*>(b + off_b);
-    float* d_s0 = initial_state ? reinterpret_cast<float*>(b + off_s0) : nullptr;
+    char* d_s0 = initial_state ? b + off_s0 : nullptr;
     int32_t* d_cu = reinterpret_cast<int32_t*>(b + off_cu);
     uint16_t* d_out = reinterpret_cast<uint16_t*>(b + off_out);
-    float* d_fin = need_fin ? reinterpret_cast<float*>(b + off_fin) : nullptr;
-    const size_t D = kda::kD, st_elems = (size_t)pr.H * D * D;  // one sequence's states
+    char* d_fin = final_state ? b + off_fin : nullptr;
+    float* d_carry = blocks ? reinterpret_cast<float*>(b + off_carry) : nullptr;
+    const char* h_s0 = static_cast<const char*>(initial_state);
+    char* h_fin = static_cast<char*>(final_state);
     std::vector<int32_t> cu_rebased;
     std::vector<size_t> cu_at(P, 0);
     if (pr.varlen) {
@@ -862,8 +880,8 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
             (e = h2d(d_v + t0 * tv, v + t0 * tv, nt * tv * 2)) ||
             (e = h2d(d_g + t0 * tv, g + t0 * tv, nt * tv * 4)) ||
             (e = h2d(d_beta + t0 * pr.H, beta + t0 * pr.H, nt * pr.H * 2)) ||
-            (initial_state && (e = h2d(d_s0 + s_first * st_elems, initial_state + s_first * st_elems,
-                                       s_count * st_elems * 4))) ||
+            (initial_state && (e = h2d(d_s0 + s_first * st_elems * se, h_s0 + s_first * st_elems * se,
+                                       s_count * st_elems * se))) ||
             (e = cudaEventRecord(hp->in_done[i], hp->in)))
             return drain(cuda_fail(e, "cudaMemcpyAsync host->device"));
     }
@@ -880,13 +898,33 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
             pp.N = pc.n1 - pc.n0;
         }
         const size_t t0 = (size_t)pc.t0, n0 = blocks ? 0 : (size_t)pc.n0;
-        const float* s0 = blocks ? (i == 0 ? d_s0 : d_fin) : (d_s0 ? d_s0 + n0 * st_elems : nullptr);
-        float* sfin = d_fin ? d_fin + n0 * st_elems : nullptr;
+        // Token blocks: the first reads the caller's initial state, later ones the fp32
+        // carry; every block but the last writes the carry, the last the final state.
+        const void* s0 = nullptr;
+        void* sfin = nullptr;
+        int32_t s0_bf = sbf, fin_bf = sbf;
+        if (blocks) {
+            if (i > 0) {
+                s0 = d_carry;
+                s0_bf = 0;
+            } else {
+                s0 = d_s0;
+            }
+            if (i < P - 1) {
+                sfin = d_carry;
+                fin_bf = 0;
+            } else {
+                sfin = d_fin;
+            }
+        } else {
+            s0 = d_s0 ? d_s0 + n0 * st_elems * se : nullptr;
+            sfin = d_fin ? d_fin + n0 * st_elems * se : nullptr;
+        }
         if ((e = cudaStreamWaitEvent(stream, hp->in_done[i], 0)))
             return drain(cuda_fail(e, "cudaStreamWaitEvent"));
         st = run(pp, d_q + t0 * pr.Hq * D, d_k + t0 * pr.Hk * D, d_v + t0 * pr.H * D,
-                 d_g + t0 * pr.H * D, d_beta + t0 * pr.H, scale, s0,
-                 pr.varlen ? d_cu + cu_at[i] : nullptr, d_out + t0 * pr.Ho * D, sfin, stream,
+                 d_g + t0 * pr.H * D, d_beta + t0 * pr.H, scale, s0, s0_bf,
+                 pr.varlen ? d_cu + cu_at[i] : nullptr, d_out + t0 * pr.Ho * D, sfin, fin_bf, stream,
                  piece_mode, seg_len, wait_limit, debug_flags);
         if (st != KDA_OK) return drain(st);
         if ((e = cudaEventRecord(hp->computed[i], stream)))
@@ -904,8 +942,8 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
             return drain(cuda_fail(e, "cudaMemcpyAsync device->host (out)"));
         const bool fin_now = final_state && (blocks ? i == P - 1 : pc.n1 > pc.n0);
         const size_t n0 = blocks ? 0 : (size_t)pc.n0, nn = blocks ? 1 : (size_t)(pc.n1 - pc.n0);
-        if (fin_now && (e = cudaMemcpyAsync(final_state + n0 * st_elems, d_fin + n0 * st_elems,
-                                            nn * st_elems * 4, cudaMemcpyDeviceToHost, hp->out)))
+        if (fin_now && (e = cudaMemcpyAsync(h_fin + n0 * st_elems * se, d_fin + n0 * st_elems * se,
+                                            nn * st_elems * se, cudaMemcpyDeviceToHost, hp->out)))
             return drain(cuda_fail(e, "cudaMemcpyAsync device->host (final_state)"));
     }
     if ((e = cudaEventRecord(hp->out_done, hp->out)) || (e = cudaStreamWaitEvent(stream, hp->out_done, 0)))
@@ -1140,7 +1178,7 @@ extern "C" kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const 
 
     kda::FwdParams p;
     kda::TensorMaps maps;
-    if ((st = prepare_call(pr, q, k, v, g, beta, scale, initial_state, nullptr, out, final_state,
+    if ((st = prepare_call(pr, q, k, v, g, beta, scale, initial_state, 0, nullptr, out, final_state, 0,
                            kDefaultWaitLimit, 0, di->status, &p, &maps)) != KDA_OK)
         return st;
     if (sp.nseg <= 1) {  // one segment: the plain serial pass, no scratch

@@ -909,10 +909,18 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (p.flags & kFlagIdentityS0) {
 #pragma unroll
                 for (int i = 0; i < 64; ++i) sreg[i] = (64 * hf + i == j) ? __float_as_uint(1.f) : 0u;
-            } else {
+            } else if (p.s0 == nullptr) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) sreg[i] = 0u;
+            } else if (p.s0_bf16) {  // bf16 states: widened exactly
+                const __nv_bfloat16* s0h = static_cast<const __nv_bfloat16*>(p.s0);
 #pragma unroll
                 for (int i = 0; i < 64; ++i)
-                    sreg[i] = p.s0 ? __float_as_uint(p.s0[soff + (size_t)(64 * hf + i) * kD + j]) : 0u;
+                    sreg[i] = __float_as_uint(__bfloat162float(s0h[soff + (size_t)(64 * hf + i) * kD + j]));
+            } else {
+                const float* s0f = static_cast<const float*>(p.s0);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) sreg[i] = __float_as_uint(s0f[soff + (size_t)(64 * hf + i) * kD + j]);
             }
             tmem_st32(tS, sreg);
             tmem_st32(tS + 32, sreg + 32);
@@ -1047,9 +1055,16 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_ld32(tS, sreg);
                 tmem_ld32(tS + 32, sreg + 32);
                 tmem_wait_ld_regs<64>(sreg);
+                if (p.sfin_bf16) {  // bf16 states: rounded to nearest even
+                    __nv_bfloat16* fh = static_cast<__nv_bfloat16*>(p.sfin);
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    p.sfin[foff + (size_t)(64 * hf + i) * kD + j] = __uint_as_float(sreg[i]);
+                    for (int i = 0; i < 64; ++i)
+                        fh[foff + (size_t)(64 * hf + i) * kD + j] = __float2bfloat16_rn(__uint_as_float(sreg[i]));
+                } else {
+                    float* ff = static_cast<float*>(p.sfin);
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) ff[foff + (size_t)(64 * hf + i) * kD + j] = __uint_as_float(sreg[i]);
+                }
             } else if (nchunks > 0 && !fin) {
                 *k2fail = 1;
             }

@@ -24,8 +24,8 @@ struct FwdParams {
     const __nv_bfloat16* v;
     const float* g;
     const __nv_bfloat16* beta;
-    const float* s0;      // [N][H][128][128] or nullptr (zero state)
-    float* sfin;          // [N][H][128][128] or nullptr (not written)
+    const void* s0;       // [N][H][128][128] fp32 (bf16 when s0_bf16), or nullptr (zero state)
+    void* sfin;           // [N][H][128][128] fp32 (bf16 when sfin_bf16), or nullptr (not written)
     __nv_bfloat16* out;   // [T_total][H][128]
     const int32_t* cu;    // [N + 1] or nullptr (dense)
     int64_t T_total;
@@ -172,7 +172,8 @@ cudaError_t launch_segment_table(const int32_t* cu, int32_t N, int64_t T_total, 
 // Dense: B sequences of nseg segments.  Varlen (seg_start != nullptr): B = N sequences,
 // each with its own count from the table; summaries and carries indexed by segment row.
 // The carry's columns are split over merge_block_cols(B, H, sm_count)-wide blocks.
-cudaError_t launch_merge(const float* m_seg, const float* b_seg, const float* s0, float* carries,
+// s0: fp32, or bf16 when s0_bf16 (the caller's initial states); carries stay fp32.
+cudaError_t launch_merge(const float* m_seg, const float* b_seg, const void* s0, int s0_bf16, float* carries,
                          int32_t B, int32_t nseg, int32_t H, int sm_count, cudaStream_t stream,
                          const int32_t* seg_start = nullptr);
 int merge_block_cols(int32_t B, int32_t H, int sm_count);

@@ -51,7 +51,7 @@ __device__ __forceinline__ void cp_async_wait() {
 template <int kCols>
 __global__ void __launch_bounds__(kMergeThreads)
 kda_merge_kernel(const float* __restrict__ m_seg, const float* __restrict__ b_seg,
-                 const float* __restrict__ s0, float* __restrict__ carries, int B, int nseg,
+                 const void* __restrict__ s0, int s0_bf16, float* __restrict__ carries, int B, int nseg,
                  int H, const int32_t* __restrict__ seg_start) {
     using S = MergeShape<kCols>;
     extern __shared__ __align__(16) float sm[];
@@ -106,7 +106,10 @@ kda_merge_kernel(const float* __restrict__ m_seg, const float* __restrict__ b_se
     // carry_0
     for (int e = tid; e < kD * kCols; e += kMergeThreads) {
         const int k = e / kCols, c = e % kCols;
-        const float v = s0 ? s0[((size_t)b * H + h) * st + (size_t)k * kD + cb * kCols + c] : 0.f;
+        const size_t i0 = ((size_t)b * H + h) * st + (size_t)k * kD + cb * kCols + c;
+        const float v = s0 == nullptr ? 0.f
+                        : s0_bf16     ? __bfloat162float(static_cast<const __nv_bfloat16*>(s0)[i0])
+                                      : static_cast<const float*>(s0)[i0];
         Cb[k * S::kBRow + c] = v;
         carry_at(0)[(size_t)k * kD + cb * kCols + c] = v;
     }
@@ -183,12 +186,12 @@ cudaError_t merge_set_smem() {
 }
 
 template <int kCols>
-cudaError_t merge_launch(const float* m_seg, const float* b_seg, const float* s0, float* carries,
+cudaError_t merge_launch(const float* m_seg, const float* b_seg, const void* s0, int s0_bf16, float* carries,
                          int32_t B, int32_t nseg, int32_t H, cudaStream_t stream,
                          const int32_t* seg_start) {
     const long long blocks = (long long)B * H * (kD / kCols);
     kda_merge_kernel<kCols><<<(unsigned)blocks, kMergeThreads, MergeShape<kCols>::kSmem, stream>>>(
-        m_seg, b_seg, s0, carries, B, nseg, H, seg_start);
+        m_seg, b_seg, s0, s0_bf16, carries, B, nseg, H, seg_start);
     return cudaGetLastError();
 }
 
@@ -207,14 +210,14 @@ int merge_block_cols(int32_t B, int32_t H, int sm_count) {
     return 8;
 }
 
-cudaError_t launch_merge(const float* m_seg, const float* b_seg, const float* s0, float* carries,
+cudaError_t launch_merge(const float* m_seg, const float* b_seg, const void* s0, int s0_bf16, float* carries,
                          int32_t B, int32_t nseg, int32_t H, int sm_count, cudaStream_t stream,
                          const int32_t* seg_start) {
     if ((long long)B * H == 0) return cudaSuccess;
     switch (merge_block_cols(B, H, sm_count)) {
-        case 32: return merge_launch<32>(m_seg, b_seg, s0, carries, B, nseg, H, stream, seg_start);
-        case 16: return merge_launch<16>(m_seg, b_seg, s0, carries, B, nseg, H, stream, seg_start);
-        default: return merge_launch<8>(m_seg, b_seg, s0, carries, B, nseg, H, stream, seg_start);
+        case 32: return merge_launch<32>(m_seg, b_seg, s0, s0_bf16, carries, B, nseg, H, stream, seg_start);
+        case 16: return merge_launch<16>(m_seg, b_seg, s0, s0_bf16, carries, B, nseg, H, stream, seg_start);
+        default: return merge_launch<8>(m_seg, b_seg, s0, s0_bf16, carries, B, nseg, H, stream, seg_start);
     }
 }
 

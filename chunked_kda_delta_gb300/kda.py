@@ -56,7 +56,7 @@ class KdaShape(ctypes.Structure):
 class KdaOptions(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("segment_len", ctypes.c_int32),
                 ("wait_limit", ctypes.c_int64), ("debug_flags", ctypes.c_int32),
-                ("host_pieces", ctypes.c_int32)]
+                ("host_pieces", ctypes.c_int32), ("state_dtype", ctypes.c_int32)]
 
 
 _lib = None
@@ -143,7 +143,8 @@ def _out_shape(q: torch.Tensor, v: torch.Tensor):
     return tuple(q.shape[:-2]) + (max(q.shape[-2], v.shape[-2]), q.shape[-1])
 
 
-def _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, device_type):
+def _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, device_type,
+                   state_dtypes=(torch.float32,)):
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
                         ("v", v, torch.bfloat16), ("g", g, torch.float32),
                         ("beta", beta, torch.bfloat16)):
@@ -165,8 +166,9 @@ def _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, device_type):
     if beta.shape != v.shape[:-1]:
         raise ValueError("beta must have v's shape without the last dim")
     if initial_state is not None:
-        if initial_state.dtype != torch.float32 or not initial_state.is_contiguous():
-            raise ValueError("initial_state must be contiguous float32")
+        if initial_state.dtype not in state_dtypes or not initial_state.is_contiguous():
+            raise ValueError("initial_state must be contiguous, one of " +
+                             ", ".join(str(d) for d in state_dtypes))
         if initial_state.device.type != device_type:
             raise ValueError(f"initial_state must be on {device_type}")
     if cu_seqlens is not None:
@@ -190,9 +192,24 @@ def _check_result(name, t, shape, dtype, device_type):
 DEBUG_STALL_WAIT = 1
 
 
-def _options(mode, segment_len, wait_limit, debug_flags=0, host_pieces=0):
+def _options(mode, segment_len, wait_limit, debug_flags=0, host_pieces=0,
+             state_dtype=torch.float32):
     return KdaOptions(int(mode), int(segment_len), int(wait_limit), int(debug_flags),
-                      int(host_pieces))
+                      int(host_pieces), 1 if state_dtype == torch.bfloat16 else 0)
+
+
+def _state_dtype(state_dtype, *given):
+    """The prefill's state type: as asked, else that of the state tensors given, else fp32;
+    every given state must have it."""
+    ts = [t for t in given if t is not None]
+    if state_dtype is None:
+        state_dtype = ts[0].dtype if ts else torch.float32
+    if state_dtype not in _STATE_DTYPES:
+        raise ValueError("state_dtype must be torch.float32 or torch.bfloat16")
+    for t in ts:
+        if t.dtype != state_dtype:
+            raise ValueError(f"states must all be {state_dtype}, got {t.dtype}")
+    return state_dtype
 
 
 def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
@@ -203,12 +220,13 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
                 final_state: Optional[torch.Tensor] = None,
                 stream=None, output_final_state: bool = False,
                 mode: int = MODE_SERIAL, segment_len: int = 0, wait_limit: int = 0,
-                debug_flags: int = 0):
+                debug_flags: int = 0, state_dtype: Optional[torch.dtype] = None):
     """KDA forward prefill on CUDA tensors; returns ``(out, final_state)``.
 
     q, k, v: bf16 ``[T, H, 128]`` (or ``[B, T, H, 128]`` dense); g: fp32 of the
-    same shape; beta: bf16 ``[T, H]``; initial_state / final_state: fp32
-    ``[N, H, 128, 128]``; cu_seqlens: int32 ``[N + 1]`` on the device.  Grouped heads:
+    same shape; beta: bf16 ``[T, H]``; initial_state / final_state: ``[N, H, 128, 128]``
+    in fp32 or bf16 (``state_dtype``, else the type of the states given, else fp32; the
+    arithmetic is fp32 either way); cu_seqlens: int32 ``[N + 1]`` on the device.  Grouped heads:
     q may have Hq heads, Hq a multiple or a divisor of v's H (k then has min(Hq, H)
     heads, the output max(Hq, H)).  ``out``
     is allocated when not given; ``final_state`` is allocated when
@@ -217,23 +235,24 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
     ``stream`` (a ``torch.cuda.Stream``, a raw handle, or the current stream).
     """
     lib = load_library()
-    _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, "cuda")
+    sdt = _state_dtype(state_dtype, initial_state, final_state)
+    _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, "cuda", _STATE_DTYPES)
     shape = _shape_of(q, v, cu_seqlens)
     N = shape.num_seqs if cu_seqlens is not None else shape.batch
     if scale is None:
         scale = shape.head_dim ** -0.5
     _check_result("out", out, _out_shape(q, v), torch.bfloat16, "cuda")
-    _check_result("final_state", final_state, (N, shape.num_heads, 128, 128), torch.float32, "cuda")
+    _check_result("final_state", final_state, (N, shape.num_heads, 128, 128), sdt, "cuda")
     if out is None:
         out = torch.empty(_out_shape(q, v), dtype=q.dtype, device=q.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, shape.num_heads, shape.head_dim, shape.head_dim),
-                                  dtype=torch.float32, device=q.device)
+                                  dtype=sdt, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif isinstance(stream, torch.cuda.Stream):
         stream = stream.cuda_stream
-    opts = _options(mode, segment_len, wait_limit, debug_flags)
+    opts = _options(mode, segment_len, wait_limit, debug_flags, state_dtype=sdt)
     with torch.cuda.device(q.device):
         st = lib.kda_prefill_ex(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                 _ptr(beta), ctypes.c_float(scale), _ptr(initial_state),
@@ -251,7 +270,7 @@ def kda_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
                      final_state: Optional[torch.Tensor] = None,
                      stream=None, output_final_state: bool = False, device=None,
                      mode: int = MODE_SERIAL, segment_len: int = 0, wait_limit: int = 0,
-                     host_pieces: int = 0):
+                     host_pieces: int = 0, state_dtype: Optional[torch.dtype] = None):
     """End-to-end prefill on HOST (CPU) tensors: copy in, compute, copy out, synchronise.
 
     Same arguments as :func:`kda_prefill` but every tensor lives in host memory
@@ -260,25 +279,26 @@ def kda_prefill_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch
     and kernels overlap.
     """
     lib = load_library()
-    _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, "cpu")
+    sdt = _state_dtype(state_dtype, initial_state, final_state)
+    _check_tensors(q, k, v, g, beta, initial_state, cu_seqlens, "cpu", _STATE_DTYPES)
     shape = _shape_of(q, v, cu_seqlens)
     N = shape.num_seqs if cu_seqlens is not None else shape.batch
     if scale is None:
         scale = shape.head_dim ** -0.5
     _check_result("out", out, _out_shape(q, v), torch.bfloat16, "cpu")
-    _check_result("final_state", final_state, (N, shape.num_heads, 128, 128), torch.float32, "cpu")
+    _check_result("final_state", final_state, (N, shape.num_heads, 128, 128), sdt, "cpu")
     if out is None:
         out = torch.empty(_out_shape(q, v), dtype=q.dtype, pin_memory=q.is_pinned())
     if final_state is None and output_final_state:
         final_state = torch.empty((N, shape.num_heads, shape.head_dim, shape.head_dim),
-                                  dtype=torch.float32, pin_memory=q.is_pinned())
+                                  dtype=sdt, pin_memory=q.is_pinned())
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
         torch.device(device)
     if stream is None:
         stream = torch.cuda.current_stream(dev).cuda_stream
     elif isinstance(stream, torch.cuda.Stream):
         stream = stream.cuda_stream
-    opts = _options(mode, segment_len, wait_limit, host_pieces=host_pieces)
+    opts = _options(mode, segment_len, wait_limit, host_pieces=host_pieces, state_dtype=sdt)
     with torch.cuda.device(dev):
         st = lib.kda_prefill_host(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                   _ptr(beta), ctypes.c_float(scale), _ptr(initial_state),

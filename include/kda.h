@@ -101,6 +101,15 @@ typedef struct kda_shape {
 #define KDA_MODE_SEGMENT 1  /* segment-parallel: pre_scan -> merge -> segment-K2 (dense or packed varlen) */
 #define KDA_MODE_AUTO 2     /* library picks serial or segment from the shape */
 
+/* State storage types (kda_options.state_dtype, kda_decode).  A bf16 final state is
+ * what the reference facade returns (flashinfer PR #4313 "feat(cake_kda): share recurrent
+ * prefill kernels across SM100 family", review of kda_prefill.py).  The arithmetic stays
+ * fp32 either way: a bf16 initial state is widened exactly on load, a bf16 final state
+ * rounded to nearest even on store, and the prefill's own carries between segments or
+ * host token blocks stay fp32. */
+#define KDA_STATE_F32 0   /* fp32 [N][H][128][128] */
+#define KDA_STATE_BF16 1  /* bf16 [N][H][128][128] */
+
 typedef struct kda_options {
     int32_t mode;         /* KDA_MODE_* (default serial) */
     int32_t segment_len;  /* segment mode: tokens per segment, multiple of 16; 0 = 8192 */
@@ -109,6 +118,9 @@ typedef struct kda_options {
     int32_t host_pieces;  /* kda_prefill_host: pieces the call is streamed in, 0..64;
                              0 = the library's choice, 1 = one piece; ignored by the
                              device entry points */
+    int32_t state_dtype;  /* KDA_STATE_F32 (0, the default) or KDA_STATE_BF16: the type of
+                             both initial_state and final_state of kda_prefill_ex and
+                             kda_prefill_host */
 } kda_options;
 
 /* debug_flags bit: the kernel's first state-pipeline wait is on a barrier that nothing
@@ -136,17 +148,20 @@ kda_status kda_prefill(const kda_shape* shape, const uint16_t* q, const uint16_t
                        const float* initial_state, const int32_t* cu_seqlens, uint16_t* out,
                        float* final_state, void* stream);
 
-/* kda_prefill_ex -- kda_prefill with options (mode, segment length, wait limit).
- * opts == NULL behaves as kda_prefill.  Segment mode takes dense or packed varlen
- * input; segment_len must be a positive multiple of 16. */
+/* kda_prefill_ex -- kda_prefill with options (mode, segment length, wait limit, state
+ * type).  opts == NULL behaves as kda_prefill.  Segment mode takes dense or packed varlen
+ * input; segment_len must be a positive multiple of 16.  initial_state and final_state
+ * point at states of opts->state_dtype (fp32 by default; [N][H][128][128] either way),
+ * with the aliasing rule of kda_prefill. */
 kda_status kda_prefill_ex(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
                           const uint16_t* v, const float* g, const uint16_t* beta, float scale,
-                          const float* initial_state, const int32_t* cu_seqlens, uint16_t* out,
-                          float* final_state, void* stream, const kda_options* opts);
+                          const void* initial_state, const int32_t* cu_seqlens, uint16_t* out,
+                          void* final_state, void* stream, const kda_options* opts);
 
 /* kda_prefill_host -- the same computation on HOST buffers, end to end.
  * Every tensor pointer (including cu_seqlens) is a host pointer with the
- * layouts above; page-locked memory gives full copy bandwidth.  The call
+ * layouts above, the states of opts->state_dtype as in kda_prefill_ex; page-locked
+ * memory gives full copy bandwidth.  The call
  * copies the inputs into a library-owned device arena, runs the prefill on
  * `stream`, copies out (and final_state when non-NULL) back, and synchronises
  * `stream` before returning.
@@ -165,8 +180,8 @@ kda_status kda_prefill_ex(const kda_shape* shape, const uint16_t* q, const uint1
  *   same stream from several threads are not supported. */
 kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uint16_t* k,
                             const uint16_t* v, const float* g, const uint16_t* beta,
-                            float scale, const float* initial_state,
-                            const int32_t* cu_seqlens, uint16_t* out, float* final_state,
+                            float scale, const void* initial_state,
+                            const int32_t* cu_seqlens, uint16_t* out, void* final_state,
                             void* stream, const kda_options* opts);
 
 /* kda_prefill_segment_noalloc -- segment-parallel prefill that allocates no device
@@ -195,10 +210,7 @@ kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q
                                        const float* initial_state, uint16_t* out,
                                        float* final_state, int32_t segment_len, void* stream);
 
-/* State storage types of kda_decode. */
-#define KDA_STATE_F32 0   /* fp32 [N][H][128][128] */
-#define KDA_STATE_BF16 1  /* bf16 [N][H][128][128]; arithmetic stays fp32, the state is
-                             rounded to bf16 (nearest even) after every token */
+/* (kda_decode with KDA_STATE_BF16 rounds the state to bf16 after every token.) */
 
 /* kda_decode -- the recurrent step for a few tokens (typically one) of each sequence,
  * the inner step of autoregressive decoding: per (sequence, head) and token, the

@@ -100,6 +100,21 @@ def test_options_rules(lib):
     assert _call(lib, s, opts=KdaOptions(0, 0, 0, 0, 65)) == INVALID   # host_pieces > 64
     # host_pieces is a host-entry setting; the device entry points accept and ignore it
     assert _call(lib, s, opts=KdaOptions(0, 0, 0, 0, 8)) not in (INVALID, ALIAS)
+    assert _call(lib, s, opts=KdaOptions(0, 0, 0, 0, 0, 2)) == INVALID  # unknown state_dtype
+    assert _call(lib, s, opts=KdaOptions(0, 0, 0, 0, 0, 1)) not in (INVALID, ALIAS)
+
+
+def test_state_dtype_sizes_the_aliasing_checks(lib):
+    # 4 heads of one sequence: fp32 states take 4 * 64 KiB, bf16 states 4 * 32 KiB.  A final
+    # state right after a bf16 initial state is clear of it, but overlaps an fp32 one.
+    s = KdaShape(1, 16, 0, 4, 128)
+    s0, fin = 0x70000000, 0x70000000 + 4 * 128 * 128 * 2
+    bf16 = KdaOptions(0, 0, 0, 0, 0, 1)
+    assert _call(lib, s, s0=s0, fin=fin, opts=bf16) not in (INVALID, ALIAS)
+    assert _call(lib, s, s0=s0, fin=fin) == ALIAS
+    assert _call(lib, s, s0=s0, fin=fin, opts=KdaOptions(0, 0, 0, 0, 0, 0)) == ALIAS
+    # the exact alias (in-place update) stays allowed for either type
+    assert _call(lib, s, s0=s0, fin=s0, opts=bf16) not in (INVALID, ALIAS)
 
 
 def test_aliasing_rules(lib):
