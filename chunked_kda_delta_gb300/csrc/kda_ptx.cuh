@@ -409,65 +409,3 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t x) {
 }
 }  // namespace ptx
 }  // namespace kda
-
-// ---------------------------------------------------------------- additions for the block kernel
-namespace kda {
-namespace ptx {
-// Instruction descriptor of kind::f16 (bf16 A and B, fp32 D, shape M x N) with the
-// operand-major bits: bit 15 = A MN-major, bit 16 = B MN-major; bit 14 negates B.
-constexpr uint32_t kIdescAMn = 1u << 15, kIdescBMn = 1u << 16, kIdescNegB = 1u << 14;
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-        "%13,%14,%15,%16};" ::"r"(taddr),
-        KDA_W8(r, 0), KDA_W8(r, 8)
-        : "memory");
-}
-// Plain store into another CTA's shared memory (cluster-space address).
-__device__ __forceinline__ void st_cluster_u32(uint32_t caddr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
-}
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-}  // namespace ptx
-}  // namespace kda
-
-namespace kda {
-namespace ptx {
-// try_wait that suspends the thread in hardware until the phase completes or `ns`
-// nanoseconds pass (no issue slots are spent while suspended).
-__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-}  // namespace ptx
-}  // namespace kda
