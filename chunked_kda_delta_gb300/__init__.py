@@ -14,6 +14,7 @@ from .kda import (  # noqa: F401
     kda_release_workspaces,
     kda_workspace_bytes,
     kda_plan,
+    kda_plan_varlen,
     kda_decode,
     STATE_F32,
     STATE_BF16,

@@ -11,6 +11,7 @@
 // overlap is rejected (flashinfer PR #4351, review of the overlap checks).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -420,6 +421,60 @@ void choose_plan(const Problem& pr, int64_t resident, int32_t* mode, int32_t* se
     }
 }
 
+// Packed varlen input whose offsets the host holds (kda_prefill_host, kda_plan_varlen).
+// Same units as choose_plan: serial costs the longer of the longest chain and the
+// chains' total over the R slots; a segment plan of length L gives sequence n
+// max(1, ceil(len_n / L)) rows, its summary and transition passes run every row but each
+// sequence's last, its output pass every row, each pass in waves of R rows of at most
+// L / 16 chunks, and the merge walks the longest sequence's rows in order.  Candidates:
+// for every count n of segments of the longest sequence, the shortest multiple of 16
+// tokens covering it in n segments (at least 512).
+void choose_plan_varlen(const Problem& pr, const int32_t* cu, int64_t resident, int32_t* mode,
+                        int32_t* seg_len) {
+    *mode = KDA_MODE_SERIAL;
+    *seg_len = 0;
+    const int64_t R = resident > 0 ? resident : 1;
+    auto cdiv = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
+    int64_t maxlen = 0, total_ck = 0, max_ck = 0;
+    for (int n = 0; n < pr.N; ++n) {
+        const int64_t len = (int64_t)cu[n + 1] - cu[n];
+        maxlen = len > maxlen ? len : maxlen;
+        total_ck += cdiv(len, kda::kChunk);
+        max_ck = cdiv(len, kda::kChunk) > max_ck ? cdiv(len, kda::kChunk) : max_ck;
+    }
+    const double serial = (double)std::max(max_ck, cdiv(total_ck * pr.Ho, R));
+    double best = serial;
+    int32_t best_len = 0;
+    int64_t prev = -1;
+    for (int64_t n = 2;; ++n) {
+        const int64_t sl = cdiv(cdiv(maxlen, n), kda::kChunk) * kda::kChunk;
+        if (sl < kMinPlanSegment) break;
+        if (sl == prev || sl > ((int64_t)1 << 30) || sl >= pr.T_total) continue;
+        prev = sl;
+        const size_t ws = (size_t)3 * (size_t)(pr.N + pr.T_total / sl) * pr.H * kda::kD * kda::kD * 4;
+        if (ws > kPlanWorkspaceCap) break;  // grows with n
+        int64_t rows = 0, inner = 0, max_rows = 0;
+        for (int i = 0; i < pr.N; ++i) {
+            const int64_t len = (int64_t)cu[i + 1] - cu[i];
+            const int64_t r = len > 0 ? cdiv(len, sl) : 1;
+            rows += r;
+            inner += r - 1;
+            max_rows = r > max_rows ? r : max_rows;
+        }
+        const int64_t l = sl / kda::kChunk;
+        const double cost = (inner > 0 ? 2.0 * (double)cdiv(inner * pr.H, R) * (double)l : 0.0) +
+                            (double)cdiv(rows * pr.Ho, R) * (double)l + kMergePerSegment * (double)max_rows;
+        if (cost < best) {
+            best = cost;
+            best_len = (int32_t)sl;
+        }
+    }
+    if (best_len && best < kSegmentMargin * serial) {
+        *mode = KDA_MODE_SEGMENT;
+        *seg_len = best_len;
+    }
+}
+
 // Query heads a segment summary pass is launched with: summaries and transitions write
 // no output, so one cluster per state head does (with grouped query heads, the equal-count
 // instance, whose state head h reads k head h and an unused q head).
@@ -802,7 +857,10 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
     const Sizes sz = sizes_of(pr, se);
     // Pieces: serial plans only (segment mode needs the whole sequence in one call).
     int32_t plan_mode = mode, plan_len = 0;  // the whole problem's plan, AUTO resolved
-    if (mode == KDA_MODE_AUTO) choose_plan(pr, di->resident_clusters, &plan_mode, &plan_len);
+    if (mode == KDA_MODE_AUTO) {
+        if (pr.varlen) choose_plan_varlen(pr, cu_seqlens, di->resident_clusters, &plan_mode, &plan_len);
+        else choose_plan(pr, di->resident_clusters, &plan_mode, &plan_len);
+    }
     const int32_t asked = opts ? opts->host_pieces : 0;
     int want = 1;
     if (plan_mode == KDA_MODE_SERIAL)
@@ -811,7 +869,9 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
     bool blocks = false;
     const std::vector<HostPiece> pieces = host_pieces(pr, cu_seqlens, want, &blocks);
     const int P = (int)pieces.size();
-    const int32_t piece_mode = P > 1 ? plan_mode : mode;
+    // A resolved segment plan runs as planned (run() could not see varlen lengths).
+    const int32_t piece_mode = (P > 1 || plan_mode == KDA_MODE_SEGMENT) ? plan_mode : mode;
+    const int32_t piece_len = (mode == KDA_MODE_AUTO && plan_mode == KDA_MODE_SEGMENT) ? plan_len : seg_len;
 
     // Device arena: the whole problem's tensors at their natural offsets, the offsets of
     // every piece rebased to its first token, the final states (the caller's type) and,
@@ -925,7 +985,7 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
         st = run(pp, d_q + t0 * pr.Hq * D, d_k + t0 * pr.Hk * D, d_v + t0 * pr.H * D,
                  d_g + t0 * pr.H * D, d_beta + t0 * pr.H, scale, s0, s0_bf,
                  pr.varlen ? d_cu + cu_at[i] : nullptr, d_out + t0 * pr.Ho * D, sfin, fin_bf, stream,
-                 piece_mode, seg_len, wait_limit, debug_flags);
+                 piece_mode, piece_len, wait_limit, debug_flags);
         if (st != KDA_OK) return drain(st);
         if ((e = cudaEventRecord(hp->computed[i], stream)))
             return drain(cuda_fail(e, "cudaEventRecord"));
@@ -987,6 +1047,24 @@ kda_status kda_plan(const kda_shape* shape, int32_t varlen, int32_t resident_clu
     kda_status st = validate_shape(shape, varlen != 0, &pr);
     if (st != KDA_OK) return st;
     choose_plan(pr, resident_clusters, mode, segment_len);
+    return KDA_OK;
+}
+
+kda_status kda_plan_varlen(const kda_shape* shape, const int32_t* host_cu_seqlens, int32_t resident_clusters,
+                           int32_t* mode, int32_t* segment_len) {
+    t_last_error[0] = '\0';
+    if (!mode || !segment_len) return fail(KDA_ERR_INVALID_ARGUMENT, "mode or segment_len is NULL");
+    if (resident_clusters < 1) return fail(KDA_ERR_INVALID_ARGUMENT, "resident_clusters must be >= 1");
+    if (!host_cu_seqlens) return fail(KDA_ERR_INVALID_ARGUMENT, "host_cu_seqlens is NULL");
+    Problem pr{};
+    kda_status st = validate_shape(shape, true, &pr);
+    if (st != KDA_OK) return st;
+    if (host_cu_seqlens[0] != 0 || host_cu_seqlens[pr.N] != pr.T_total)
+        return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must start at 0 and end at T_total");
+    for (int n = 0; n < pr.N; ++n)
+        if (host_cu_seqlens[n + 1] < host_cu_seqlens[n])
+            return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must be non-decreasing");
+    choose_plan_varlen(pr, host_cu_seqlens, resident_clusters, mode, segment_len);
     return KDA_OK;
 }
 

@@ -13,6 +13,7 @@ import os
 import threading
 from typing import Optional
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -31,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "kda_prefill", "kda_prefill_ex", "kda_prefill_host", "kda_workspace_bytes",
     "kda_get_device_status", "kda_release_workspaces", "kda_status_string",
     "kda_last_error_message", "kda_version", "kda_prefill_segment_noalloc", "kda_plan",
-    "kda_decode",
+    "kda_plan_varlen", "kda_decode",
 )
 
 STATE_F32 = 0
@@ -89,6 +90,8 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = False) -> 
             f32p, ctypes.c_int32, vp]
         lib.kda_workspace_bytes.argtypes = [ctypes.POINTER(KdaShape), ctypes.POINTER(KdaOptions),
                                             ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_plan_varlen.argtypes = [ctypes.POINTER(KdaShape), vp, ctypes.c_int32,
+                                        ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         lib.kda_plan.argtypes = [ctypes.POINTER(KdaShape), ctypes.c_int32, ctypes.c_int32,
                                  ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         lib.kda_decode.argtypes = [ctypes.POINTER(KdaShape), u16p, u16p, u16p, f32p, u16p,
@@ -331,6 +334,20 @@ def kda_plan(batch: int, seq_len: int, num_heads: int, resident_clusters: int,
     mode, seg = ctypes.c_int32(0), ctypes.c_int32(0)
     _check(lib, lib.kda_plan(ctypes.byref(shape), int(bool(varlen)), int(resident_clusters),
                              ctypes.byref(mode), ctypes.byref(seg)))
+    return int(mode.value), int(seg.value)
+
+
+def kda_plan_varlen(seq_lens, num_heads: int, resident_clusters: int, head_dim: int = 128,
+                    num_q_heads: int = 0):
+    """The (mode, segment_len) that ``MODE_AUTO`` of :func:`kda_prefill_host` picks for a
+    packed batch with these sequence lengths.  Host only."""
+    lib = load_library()
+    lens = [int(x) for x in seq_lens]
+    cu = (ctypes.c_int32 * (len(lens) + 1))(*([0] + list(np.cumsum(lens, dtype=np.int64))))
+    shape = KdaShape(1, int(sum(lens)), len(lens), num_heads, head_dim, num_q_heads)
+    mode, seg = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib, lib.kda_plan_varlen(ctypes.byref(shape), ctypes.cast(cu, ctypes.c_void_p),
+                                    int(resident_clusters), ctypes.byref(mode), ctypes.byref(seg)))
     return int(mode.value), int(seg.value)
 
 

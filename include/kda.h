@@ -272,6 +272,19 @@ kda_status kda_workspace_bytes(const kda_shape* shape, const kda_options* opts, 
 kda_status kda_plan(const kda_shape* shape, int32_t varlen, int32_t resident_clusters, int32_t* mode,
                     int32_t* segment_len);
 
+/* kda_plan_varlen -- the plan for packed varlen input whose offsets the caller holds on
+ * the host (`host_cu_seqlens`, int32 [N + 1], host memory): what kda_prefill_host with
+ * KDA_MODE_AUTO runs for such input (the device entry points cannot see device-resident
+ * lengths and keep varlen input serial).  Same units as kda_plan: serial costs the longer
+ * of the longest chain and all chains over the resident clusters; a segment plan of
+ * length L gives sequence n max(1, ceil(len_n / L)) segment rows (segment-parallel
+ * prefill for packed batches, cuLA PR #103 "intracard-CP prefill", planner notes), its two
+ * summary passes run every row but each sequence's last, and segment mode is chosen only
+ * when it beats serial by 20%.  Host only.  Errors: KDA_ERR_INVALID_ARGUMENT for a bad
+ * shape (varlen rules), NULL pointers, malformed offsets or resident_clusters < 1. */
+kda_status kda_plan_varlen(const kda_shape* shape, const int32_t* host_cu_seqlens, int32_t resident_clusters,
+                           int32_t* mode, int32_t* segment_len);
+
 /* Reads and clears the device status word of the current device after
  * synchronising `stream`.  *code receives KDA_OK, KDA_ERR_INVALID_ARGUMENT
  * (malformed cu_seqlens contents seen by a kernel) or KDA_ERR_DEVICE_TIMEOUT.

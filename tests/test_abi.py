@@ -324,3 +324,25 @@ def test_binding_refuses_short_outputs():
         K.kda_prefill_host(q, q, v, g, b, out=torch.zeros(16, 2, 128, dtype=torch.bfloat16))
     with pytest.raises(ValueError):
         K.kda_prefill_host(q, q, v, g, b, final_state=torch.zeros(1, 2, 128, 128))
+
+
+def test_varlen_planner(lib):
+    """kda_plan_varlen: equal-length batches get the dense plan; many or short sequences
+    stay serial; a few long ones are split; malformed offsets are refused."""
+    from chunked_kda_delta_gb300.inputs import varlen_h12_lengths
+    R = 76
+    for T, H in [(131072, 4), (65536, 2), (8192, 12), (32768, 3)]:
+        assert K.kda_plan_varlen([T], H, R) == K.kda_plan(1, T, H, R)
+    assert K.kda_plan_varlen([65536, 65536], 4, R) == K.kda_plan(2, 65536, 4, R)
+    assert K.kda_plan_varlen(varlen_h12_lengths(3), 12, R) == (K.MODE_SERIAL, 0)
+    assert K.kda_plan_varlen([512] * 32, 12, R) == (K.MODE_SERIAL, 0)
+    assert K.kda_plan_varlen([100, 0, 37], 4, R) == (K.MODE_SERIAL, 0)
+    m, s = K.kda_plan_varlen([20000, 20000], 2, R)
+    assert m == K.MODE_SEGMENT and s % 16 == 0 and 512 <= s < 20000
+    shape = KdaShape(1, 40, 2, 2, 128)
+    mode, seg = ctypes.c_int32(0), ctypes.c_int32(0)
+    for bad in ([0, 30, 20], [1, 20, 40], [0, 20, 41]):
+        cu = (ctypes.c_int32 * 3)(*bad)
+        assert lib.kda_plan_varlen(ctypes.byref(shape), ctypes.cast(cu, ctypes.c_void_p), R,
+                                   ctypes.byref(mode), ctypes.byref(seg)) == INVALID
+    assert lib.kda_plan_varlen(ctypes.byref(shape), None, R, ctypes.byref(mode), ctypes.byref(seg)) == INVALID

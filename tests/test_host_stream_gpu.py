@@ -129,3 +129,21 @@ def test_default_pieces_on_a_large_input(orc):
     o_ref, f_ref = oracle_on_heads(orc, inp, heads)
     assert_close(to_f64_numpy(o_h.reshape(-1, 16, 128)[:, heads]), o_ref, "default pieces out")
     assert_close(to_f64_numpy(f_h[:, heads]), f_ref, "default pieces final_state")
+
+
+def test_auto_plans_varlen_segments_from_host_offsets(orc):
+    """The host entry sees packed offsets on the host: AUTO runs two long sequences of a
+    packed batch as a segment plan (kda_plan_varlen's pick) and matches the oracle, every
+    element, with slow-decay gates so the carries between segments matter."""
+    lens, H = [20000, 3, 19984], 2
+    mode, seg = K.kda_plan_varlen(lens, H, 76)
+    assert mode == K.MODE_SEGMENT
+    inp = make_inputs(custom(lens, H, True, seed=1401, dense=False), "cpu", stress=True)
+    h = {n: inp[n].pin_memory() for n in ("q", "k", "v", "g", "beta", "initial_state")}
+    out, fin = K.kda_prefill_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
+                                  initial_state=h["initial_state"], cu_seqlens=inp["cu_seqlens"],
+                                  output_final_state=True, mode=K.MODE_AUTO)
+    assert K.kda_get_device_status() == 0
+    o_ref, f_ref = oracle_on_heads(orc, inp, range(H))
+    assert_close(to_f64_numpy(out), o_ref, "host AUTO varlen out")
+    assert_close(to_f64_numpy(fin), f_ref, "host AUTO varlen final state")
