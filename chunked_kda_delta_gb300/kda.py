@@ -384,8 +384,7 @@ def kda_prefill_segment_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
     scratch in a fixed 32 MiB device array shared by all calls, so ``out`` (and
     ``final_state`` when wanted) must be passed in.  Shapes needing more than
     B * H * (3 * nseg - 2) = 512 state slots are rejected; calls overlapping on the
-    GPU race on the shared array.  The first call on a device must precede any
-    stream capture.
+    GPU race on the shared array.
     """
     lib = load_library()
     _check_tensors(q, k, v, g, beta, initial_state, None, "cuda")

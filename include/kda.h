@@ -202,8 +202,8 @@ kda_status kda_prefill_host(const kda_shape* shape, const uint16_t* q, const uin
  *   reads before reading it).  Calls that overlap on the GPU (other streams, other
  *   threads) race on it: serialise them.
  *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call before any
- *   stream capture.  Every GPU that loads the library holds the 32 MiB until exit. */
+ *   (cudaGetSymbolAddress) with that device current, once.  Every GPU that loads the
+ *   library holds the 32 MiB until exit. */
 kda_status kda_prefill_segment_noalloc(const kda_shape* shape, const uint16_t* q,
                                        const uint16_t* k, const uint16_t* v, const float* g,
                                        const uint16_t* beta, float scale,
