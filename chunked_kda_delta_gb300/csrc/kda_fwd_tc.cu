@@ -86,7 +86,10 @@ constexpr uint32_t kColDA = 320;  // 2 buffers x 8 columns: delta^T bf16 pairs (
 // Input stage (K1 CTA): q, k, v bf16 [16][128]; g fp32 [16][128]; beta fp32 [16].
 constexpr int kInQ = 0, kInK = 4096, kInV = 8192, kInG = 12288, kInBeta = 20480;
 constexpr int kInBytes = 20608;
-constexpr int kInStages = 4;
+// One input stage per K1 group (chunk c -> stage c % 3 = group c % 3): successive phases
+// of a stage's barriers then belong to one group, in order, so a group never waits on a
+// phase two ahead of the last one it saw complete (a parity wait cannot tell those apart).
+constexpr int kInStages = kK1Groups;
 constexpr uint32_t kTxBytes = 20480;  // q, k, v, g tiles
 // Chunk operand stage (K1 -> K2): B1 = [W ; Qtil] (N=32, K=128), B2 = Kbar (N=128,
 // K=16), B3 = Mq (N=16, K=16), all bf16 in the no-swizzle K-major layout; U fp32 rows
@@ -137,6 +140,7 @@ enum {  // K1 CTA barriers
     BAR_IN_FULL = 0, BAR_IN_EMPTY = 4, BAR_OUT_FREE = 8,
     BAR_COPIED = BAR_OUT_FREE + kRecvStages  // per K1 group: its last bulk copy has landed
 };
+static_assert(kInStages <= BAR_IN_EMPTY - BAR_IN_FULL, "input barriers overlap");
 static_assert(BAR_COPIED + kK1Groups <= kNumBars, "too many barriers");
 enum {  // K2 CTA barriers
     BAR_K1_FULL = 0,                       // kRecvStages: chunk operands landed
@@ -364,13 +368,21 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (rank == 0 && warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // beta is read with plain loads two chunks ahead (its [T][H] rows are 2 bytes
-        // wide, below the 16-byte TMA granule) and stored next to the TMA tiles.
-        auto load_beta = [&](int cc) -> float {
-            if (lane >= kChunk || cc >= nchunks) return 0.f;
+        // wide, below the 16-byte TMA granule) and stored next to the TMA tiles.  The raw
+        // bf16 bits of chunks c and c + 1 sit in two registers (the loop is unrolled by
+        // two) until their store: no instruction reads a load result before the load has
+        // had two chunks to complete.  Widening at the load, or rotating one register
+        // into another, would make this warp wait a full global-load latency on every
+        // chunk, and its TMA issue rate would then bound every stage of the pipeline.
+        auto load_beta = [&](int cc, uint32_t& bits) {
+            bits = 0u;
             const int64_t t = bos + (int64_t)cc * kChunk + lane;
-            return t < eos ? __bfloat162float(p.beta[t * H + h]) : 0.f;
+            if (lane < kChunk && cc < nchunks && t < eos)
+                bits = *reinterpret_cast<const unsigned short*>(p.beta + (t * H + h));
         };
-        float b_cur = load_beta(0), b_next = load_beta(1);
+        uint32_t b_even, b_odd;
+        load_beta(0, b_even);
+        load_beta(1, b_odd);
         int hq = h, hk = h;  // q and k heads of this cluster, once
         if (kGrouped) {
             const HeadMap hm = head_map((int)((blockIdx.x >> 1) % (p.Hq > p.H ? p.Hq : p.H)), p.H, p.Hq);
@@ -378,19 +390,20 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             hk = hm.hk;
         }
         int issued = 0;
-        for (int c = 0; c < nchunks; ++c) {
+        // Chunk c: wait for its input stage, store its beta (`bits`), load the beta of
+        // chunk c + 2 into `bits`, issue the four tiles.  False after a timeout.
+        auto produce = [&](int c, uint32_t& bits) -> bool {
             const int s = c % kInStages;
             const bool ok = c < kInStages ||
                             mbar_wait(bar(BAR_IN_EMPTY + s), ((c / kInStages) - 1) & 1, lim);
             if (__any_sync(0xffffffffu, !ok)) {
                 if (lane == 0) record(p.status, kStatusTimeout);
-                break;
+                return false;
             }
             const uint32_t dst = sbase + kSmIn + s * kInBytes;
             if (lane < kChunk)
-                reinterpret_cast<float*>(smem + kSmIn + s * kInBytes + kInBeta)[lane] = b_cur;
-            b_cur = b_next;
-            b_next = load_beta(c + 2);
+                reinterpret_cast<float*>(smem + kSmIn + s * kInBytes + kInBeta)[lane] = __uint_as_float(bits << 16);
+            load_beta(c + 2, bits);
             __syncwarp();
             if (lane == 0) {
                 const int32_t t0 = (int32_t)(bos + (int64_t)c * kChunk);
@@ -401,6 +414,11 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tma_load_3d(dst + kInG, &tm_g, bar(BAR_IN_FULL + s), 0, h, t0);
             }
             issued = c + 1;
+            return true;
+        };
+        for (int c = 0; c < nchunks; c += 2) {
+            if (!produce(c, b_even)) break;
+            if (c + 1 < nchunks && !produce(c + 1, b_odd)) break;
         }
         // Drain: every issued load must have landed before the CTA exits.
         if (lane == 0)
