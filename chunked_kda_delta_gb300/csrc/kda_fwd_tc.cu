@@ -116,6 +116,12 @@ constexpr int kGEref = ST_NUM * kStArr, kGA = kGEref + 512, kGTb = kGA + 1024,
 constexpr int kSmIn = 0;
 constexpr int kSmGrp = kSmIn + kInStages * kInBytes;
 constexpr int kSmOutLocal = kSmGrp + kK1Groups * kGrpBytes;
+// Local operand stages (K1 CTA), chunk c -> stage c % kOutStages, shared by the groups
+// round-robin: a group writes chunk c's operands once the copy of chunk c - kOutStages
+// has landed.  The relay reports landings in chunk order, so when a group waits for that
+// copy it has already seen chunk c - kOutStages - 1 land (its own previous chunk's stage
+// wait covered it): the stage barrier is never waited on two phases ahead.
+constexpr int kOutStages = kK1Groups + 1;
 constexpr int kSmRecv = 0;
 constexpr int kSmOTile = kSmRecv + kRecvStages * kOutBytes;  // K2 CTA: 2 output tiles bf16 [16][128]
 constexpr int kOTileBytes = kChunk * kD * 2;
@@ -125,7 +131,7 @@ constexpr int kOTiles = 4;  // output tiles: a tile is rewritten 4 chunks after 
 constexpr int kSmPR = kSmOTile + kOTiles * kOTileBytes;
 constexpr int kPRBytes = 1024;
 constexpr int kPRSlots = 3;
-constexpr int kSmBar = kSmOutLocal + kK1Groups * kOutBytes;
+constexpr int kSmBar = kSmOutLocal + kOutStages * kOutBytes;
 constexpr int kNumBars = 24;
 constexpr int kSmTmemSlot = kSmBar + kNumBars * 8;
 constexpr int kSmFail = kSmTmemSlot + 8;            // int32 per K1 group: failure flags
@@ -138,10 +144,10 @@ static_assert(kSmPR + kPRSlots * kPRBytes <= kSmBar, "K2 buffers overlap the bar
 static_assert(kSmOTile % 128 == 0, "TMA store source must be 128-byte aligned");
 enum {  // K1 CTA barriers
     BAR_IN_FULL = 0, BAR_IN_EMPTY = 4, BAR_OUT_FREE = 8,
-    BAR_COPIED = BAR_OUT_FREE + kRecvStages  // per K1 group: its last bulk copy has landed
+    BAR_COPIED = BAR_OUT_FREE + kRecvStages  // per local operand stage: its last bulk copy has landed
 };
 static_assert(kInStages <= BAR_IN_EMPTY - BAR_IN_FULL, "input barriers overlap");
-static_assert(BAR_COPIED + kK1Groups <= kNumBars, "too many barriers");
+static_assert(BAR_COPIED + kOutStages <= kNumBars, "too many barriers");
 enum {  // K2 CTA barriers
     BAR_K1_FULL = 0,                       // kRecvStages: chunk operands landed
     BAR_D1 = BAR_K1_FULL + kRecvStages,    // MMA1 group of a chunk complete (2 commits)
@@ -330,7 +336,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mbar_init(bar(BAR_IN_EMPTY + s), 1);
             }
             for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_OUT_FREE + s), 1);
-            for (int gi = 0; gi < kK1Groups; ++gi) mbar_init(bar(BAR_COPIED + gi), 1);
+            for (int os = 0; os < kOutStages; ++os) mbar_init(bar(BAR_COPIED + os), 1);
             for (int gi = 0; gi < kK1Groups; ++gi) fail_flag[gi] = 0;
         } else {
             for (int s = 0; s < kRecvStages; ++s) mbar_init(bar(BAR_K1_FULL + s), 1);
@@ -451,7 +457,6 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // after the group's barrier), channel mask and exact Gram terms.
         volatile uint32_t* slow_flag = reinterpret_cast<volatile uint32_t*>(grp + kGSlow);
         float* corr = reinterpret_cast<float*>(grp + kGCorr);
-        unsigned char* ob = smem + kSmOutLocal + gi * kOutBytes;
         const float2 l2e2 = make_float2(kLog2e, kLog2e), nl2e2 = make_float2(-kLog2e, -kLog2e);
         const bool zero_v = (p.flags & kFlagZeroV) != 0;
         const bool with_out = (p.flags & kFlagNoOutput) == 0;
@@ -524,13 +529,15 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     kb1[rr >> 1] = w >> 16;
                 }
             }
-            // The local operand buffer is written from here on: the group's previous bulk
-            // copy out of it must have landed (a copy into the peer CTA completes only
-            // through the peer's barrier, which the K2 CTA relays back).  Waiting this late
-            // gives that copy the whole of phase 1 to land.
+            // The local operand stage is written from here on: the bulk copy of chunk
+            // c - kOutStages out of it must have landed (a copy into the peer CTA completes
+            // only through the peer's barrier, which the K2 CTA relays back).  Waiting this
+            // late gives that copy the whole of phase 1 to land.
+            const int lst = c % kOutStages;
+            unsigned char* ob = smem + kSmOutLocal + lst * kOutBytes;
             bool copied = true;
-            if (kt == kt_wait && c >= kK1Groups)
-                copied = mbar_wait(bar(BAR_COPIED + gi), ((c / kK1Groups) - 1) & 1, lim);
+            if (kt == kt_wait && c >= kOutStages)
+                copied = mbar_wait(bar(BAR_COPIED + lst), ((c / kOutStages) - 1) & 1, lim);
             if (named_bar_or(nbar, 128, !copied)) {
                 if (kt == kt_wait) record(p.status, kStatusTimeout);
                 break;
@@ -745,7 +752,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         break;
                     }
                     st_release_cta(landed, c + 1);
-                    mbar_arrive_remote_relaxed(mapa(bar(BAR_COPIED + c % kK1Groups), 0));
+                    mbar_arrive_remote_relaxed(mapa(bar(BAR_COPIED + c % kOutStages), 0));
                 }
             }
             __syncwarp();
