@@ -1,7 +1,7 @@
 // tcgen05_probe.cu -- test-only check of the tcgen05 building blocks used by the
-// library (shared-memory matrix descriptors of the no-swizzle K-major layout,
-// the bf16 A operand held in TMEM, TMEM loads), on a 128x128 problem whose
-// products the test recomputes on the host.  One CTA, 128 threads.
+// library (shared-memory matrix descriptors of the no-swizzle K-major layout and of the
+// 128-byte-swizzled M-major layout, the bf16 A operand held in TMEM, TMEM loads), on
+// problems whose products the test recomputes on the host.  One CTA, 128 threads.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -98,7 +98,70 @@ probe_kernel(const uint16_t* A, const uint16_t* B1, const uint16_t* B2, float* D
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 256);
 }
+// A operand stored M-major (MN-major) with the 128-byte swizzle, as a TMA load with
+// CU_TENSOR_MAP_SWIZZLE_128B writes a [K][M] bf16 tile in two boxes of 64 M-columns:
+// box h (M columns 64h .. 64h+63) at byte 2048h, row k (K index) at 128k within it, the
+// 16-byte chunk index of a row XORed with k % 8.  Descriptor: LBO = 2048 (between the
+// two 64-column boxes), SBO = 1024 (between the two 8-row K groups), swizzle mode 2.
+// D[m][n] = sum_k V[k][m] B[n][k] for M = 128, N = 16, K = 16, B K-major without swizzle.
+__global__ void __launch_bounds__(128, 1)
+probe_mn_sw128(const uint16_t* V, const uint16_t* B, float* D, int32_t* err, int64_t limit) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char* v_sm = smem;          // 2 boxes x 16 rows x 128 B = 4 KiB
+    unsigned char* b_sm = smem + 4096;   // 16 x 16, K-major
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid / 32;
+    if (tid == 0 && (smem_u32(v_sm) & 1023u) != 0) atomicExch(err, 9);  // the swizzle needs 1 KiB alignment
+    for (int e = tid; e < 16 * 128; e += 128) {
+        const int k = e / 128, m = e % 128;
+        const int box = m / 64, byte = (m % 64) * 2;
+        const int chunk = (byte / 16) ^ (k % 8);
+        *reinterpret_cast<uint16_t*>(v_sm + box * 2048 + k * 128 + chunk * 16 + byte % 16) = V[e];
+    }
+    for (int e = tid; e < 16 * 16; e += 128) {
+        const int n = e / 16, k = e % 16;
+        *reinterpret_cast<uint16_t*>(b_sm + kmajor_off(n, k, kLboK, kSboB2)) = B[e];
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_base), 32);
+        tmem_relinquish();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    if (tid == 0) {
+        const uint64_t adesc = sdesc(smem_u32(v_sm), 2048, 1024) | ((uint64_t)2 << 61);
+        mma_ss(tbase, adesc, sdesc(smem_u32(b_sm), kLboK, kSboB2), idesc_bf16(128, 16) | (1u << 15), 0);
+        tc_commit(smem_u32(&bar));
+    }
+    const bool ok = mbar_wait(smem_u32(&bar), 0, limit);
+    if (!ok) atomicExch(err, 7);
+    tc_fence_after();
+    if (ok) {
+        uint32_t r[16];
+        tmem_ld16(tbase + lane_base, r);
+        tmem_wait_ld_regs<16>(r);
+        for (int c = 0; c < 16; ++c) D[tid * 16 + c] = __uint_as_float(r[c]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 32);
+}
 }  // namespace
+
+extern "C" int tcgen05_probe_mn_sw128(const uint16_t* V, const uint16_t* B, float* D, int32_t* err) {
+    const int smem = 8192;
+    probe_mn_sw128<<<1, 128, smem>>>(V, B, D, err, 1 << 22);
+    return (int)cudaDeviceSynchronize();
+}
 
 extern "C" int tcgen05_probe(const uint16_t* A, const uint16_t* B1, const uint16_t* B2,
                              float* D1_ss, float* D1_ts, float* D2, int32_t* err) {
