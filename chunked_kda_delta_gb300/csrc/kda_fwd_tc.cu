@@ -501,7 +501,8 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const uint32_t* q2 = reinterpret_cast<const uint32_t*>(in + kInQ);
             const uint32_t* k2 = reinterpret_cast<const uint32_t*>(in + kInK);
             const uint32_t* v2 = reinterpret_cast<const uint32_t*>(in + kInV);
-            uint32_t kb0[4], kb1[4];
+            uint32_t kb0[4], kb1[4];  // Kbar rows 8hr.. of channels 2pc and 2pc+1, bf16 pairs
+            float2 kbe = make_float2(0.f, 0.f);  // Kbar of the pair's even row
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
                 const int r = 8 * hr + rr;
@@ -520,13 +521,11 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 row[ST_QQ * kStArr / 4] = pack_bf16(qq.x, qq.y);
                 row[ST_KK * kStArr / 4] = pack_bf16(kk.x, kk.y);
                 row[ST_VV * kStArr / 4] = vv;
-                const uint32_t w = pack_bf16(kb.x, kb.y);  // lo: channel 2pc, hi: 2pc+1
-                if (rr & 1) {
-                    kb0[rr >> 1] |= w << 16;
-                    kb1[rr >> 1] |= w & 0xffff0000u;
+                if (rr & 1) {  // rows rr-1 (low half) and rr (high half) of each channel
+                    kb0[rr >> 1] = pack_bf16(kbe.x, kb.x);
+                    kb1[rr >> 1] = pack_bf16(kbe.y, kb.y);
                 } else {
-                    kb0[rr >> 1] = w & 0xffffu;
-                    kb1[rr >> 1] = w >> 16;
+                    kbe = kb;
                 }
             }
             // The local operand stage is written from here on: the bulk copy of chunk
