@@ -34,13 +34,14 @@
 //   MMA2: S^T += delta^T . Kbar, after the chain scaled S^T by exp(gam_C) in place.
 //
 // Work split (416 threads per CTA, 13 warps):
-//   CTA rank 0 ("K1 CTA"): warp 0 is the TMA producer (q/k/v/g tiles into a 4-stage
-//     ring; beta with plain loads, two chunks ahead); warps 1-12 are three K1 groups of
-//     4 warps taking every third chunk (cumulative decay, decayed operands, in-chunk
-//     Grams and the WY solve, W and U; the 16x16 products use mma.sync because tcgen05's
-//     smallest M is 64).  A group writes its chunk's operands (21.8 KB) into a local
-//     buffer and ships them to the K2 CTA with one cp.async.bulk shared::cta ->
-//     shared::cluster copy that completes the K2 CTA's barrier.
+//   CTA rank 0 ("K1 CTA"): warp 0 is the TMA producer (q/k/v/g tiles into a ring with
+//     one stage per K1 group; beta with plain loads, two chunks ahead); warps 1-12 are
+//     three K1 groups of 4 warps taking every third chunk (cumulative decay, decayed
+//     operands, in-chunk Grams and the WY solve, W and U; the 16x16 products use mma.sync
+//     because tcgen05's smallest M is 64).  A group writes its chunk's operands (21.8 KB)
+//     into one of four local stages and ships them to the K2 CTA with one
+//     cp.async.bulk shared::cta -> shared::cluster copy that completes the K2 CTA's
+//     barrier.
 //   CTA rank 1 ("K2 CTA"): warps 1-8 run the state chain (decay and bf16 copy of the
 //     state, delta, output rows) and only arrive on two named barriers; warp 11 issues
 //     the state update and the Mq term, warps 10 and 9 MMA1 of the next chunk (the
@@ -111,7 +112,7 @@ enum { ST_KQ = 0, ST_QQ, ST_KK, ST_VV, ST_NUM };
 constexpr int kGEref = ST_NUM * kStArr, kGA = kGEref + 512, kGTb = kGA + 1024,
               kGBeta = kGTb + 768, kGSlow = kGBeta + 64, kGCorr = kGSlow + 32,
               kGrpBytes = kGCorr + 2048;
-// Shared memory map.  K1 CTA: input ring, 2 group scratches, 2 local operand stages.
+// Shared memory map.  K1 CTA: input ring, the group scratches, the local operand stages.
 // K2 CTA: receive ring at offset 0.  Barriers sit at the same offset in both.
 constexpr int kSmIn = 0;
 constexpr int kSmGrp = kSmIn + kInStages * kInBytes;
@@ -123,7 +124,7 @@ constexpr int kSmOutLocal = kSmGrp + kK1Groups * kGrpBytes;
 // wait covered it): the stage barrier is never waited on two phases ahead.
 constexpr int kOutStages = kK1Groups + 1;
 constexpr int kSmRecv = 0;
-constexpr int kSmOTile = kSmRecv + kRecvStages * kOutBytes;  // K2 CTA: 2 output tiles bf16 [16][128]
+constexpr int kSmOTile = kSmRecv + kRecvStages * kOutBytes;  // K2 CTA: output tiles bf16 [16][128]
 constexpr int kOTileBytes = kChunk * kD * 2;
 constexpr int kOTiles = 4;  // output tiles: a tile is rewritten 4 chunks after its store
 // K2 CTA: ring of [P ; R] lookahead operands (bf16, N = 32 x K = 16, K-major):
