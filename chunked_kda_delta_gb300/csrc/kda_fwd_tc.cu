@@ -71,7 +71,7 @@ constexpr float kFastLimit = 80.f;  // largest log-decay fall over a chunk for t
 constexpr uint32_t kTmemCols = 512;
 // Bound of the waits that drain in-flight copies and MMAs before exit; independent of
 // the caller's wait limit so that an early exit never leaves asynchronous work behind.
-constexpr int64_t kDrainLimit = 1ll << 24;
+constexpr int64_t kDrainLimit = 1ll << 22;  // rounds of at most ~1 us each
 constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM column map (K2 CTA)

@@ -29,14 +29,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  "r"(bytes)
                  : "memory");
 }
+// Suspend-time hint of every try_wait, in ns: a thread whose phase is not complete sleeps
+// up to this long (it wakes as soon as the phase completes).  Without it the hardware's
+// default window is short, and the roles that mostly wait (relay, producer, the K1
+// groups' waiting threads) poll often enough to take issue slots from the warps sharing
+// their SM sub-partition: the prefill ran 2.8% slower.  A round of a bounded wait lasts
+// at most about this long.
+constexpr uint32_t kTryWaitHintNs = 1000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kTryWaitHintNs)
         : "memory");
     return ok != 0;
 }
@@ -53,10 +60,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kTryWaitHintNs)
         : "memory");
     return ok != 0;
 }

@@ -113,7 +113,8 @@ typedef struct kda_shape {
 typedef struct kda_options {
     int32_t mode;         /* KDA_MODE_* (default serial) */
     int32_t segment_len;  /* segment mode: tokens per segment, multiple of 16; 0 = 8192 */
-    int64_t wait_limit;   /* iteration limit of each device spin wait; 0 = library default */
+    int64_t wait_limit;   /* rounds of each device barrier wait (a round sleeps at most
+                             ~1 us); 0 = library default (2^22, about 4 s) */
     int32_t debug_flags;  /* 0 in normal use; KDA_DEBUG_* bits for failure-path tests */
     int32_t host_pieces;  /* kda_prefill_host: pieces the call is streamed in, 0..64;
                              0 = the library's choice, 1 = one piece; ignored by the
