@@ -1006,7 +1006,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 // The SDONE and D1 waits pace the chain against the issuers and are taken
                 // even after a failure (the issuers then commit without MMAs).
                 bool w = !*k2fail && landed_or_wait(c);                    // U_c, exp(gam_C(c))
-                if (c > 0 && !mbar_wait(bar(BAR_SDONE), (c - 1) & 1, lim)) w = false;  // S_c complete
+                if (c > 0 && !mbar_wait_now(bar(BAR_SDONE), (c - 1) & 1, lim)) w = false;  // S_c complete
                 uint32_t pk[32];  // bf16 copy of D_{c+1}, written once MMA1(c) has read D_c
                 if (w) {
                     tc_fence_after();
@@ -1033,7 +1033,7 @@ kda_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     for (int i = 0; i < 32; ++i)
                         pk[i] = pack_bf16(__uint_as_float(sreg[2 * i]), __uint_as_float(sreg[2 * i + 1]));
                 }
-                if (!mbar_wait(bar(BAR_D1), c & 1, lim)) w = false;
+                if (!mbar_wait_now(bar(BAR_D1), c & 1, lim)) w = false;
                 {
                     if (w) {
                         tc_fence_after();

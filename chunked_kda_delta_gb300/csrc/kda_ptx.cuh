@@ -34,7 +34,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 // default window is short, and the roles that mostly wait (relay, producer, the K1
 // groups' waiting threads) poll often enough to take issue slots from the warps sharing
 // their SM sub-partition: the prefill ran 2.8% slower.  A round of a bounded wait lasts
-// at most about this long.
+// at most about this long (mbar_wait_now below is the unhinted form).
 constexpr uint32_t kTryWaitHintNs = 1000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -52,6 +52,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t limit) {
     for (int64_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// The same without the hint, for short waits on a critical path (an MMA's completion that
+// the waiting thread needs next): the hinted form wakes a little later.
+__device__ __forceinline__ bool mbar_try_wait_now(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_now(uint32_t bar, uint32_t parity, int64_t limit) {
+    for (int64_t i = 0; i < limit; ++i)
+        if (mbar_try_wait_now(bar, parity)) return true;
     return false;
 }
 
